@@ -1,0 +1,109 @@
+"""Seeded synthetic inputs shared by the CUDA path and the CPU oracle.
+
+This module holds none of the method's arithmetic: it only draws numbers and
+builds masks, so that the oracle and the GPU consume identical bytes. The
+workloads follow the attention shapes of the pages' evaluation (multi-head and
+grouped-query prefill, split-K decode, block-sparse attention with the mask
+families STOF evaluates: causal, sliding window, Longformer/Bigbird-like).
+No dataset or trained weight is involved; every tensor is drawn here.
+
+Recipe: ``torch.Generator().manual_seed(seed)`` on the CPU, ``torch.randn``
+in float32 for Q, then K, then V (in that order, from one generator),
+multiplied by ``amp`` and cast to the workload dtype.
+"""
+
+import math
+
+import numpy as np
+import torch
+
+#: The named workloads. ``tile`` is the block-sparse tile side.
+WORKLOADS = {
+    # tiny exact case, fp32 in and out
+    "tiny_fp32": dict(B=1, H=1, Hkv=1, Sq=128, Sk=128, d=64, causal=False,
+                      dtype="f32", seed=0, amp=1.0),
+    # multi-head causal prefill
+    "mha_prefill": dict(B=4, H=32, Hkv=32, Sq=4096, Sk=4096, d=128, causal=True,
+                        dtype="bf16", seed=1, amp=1.0),
+    # grouped-query long-context causal prefill
+    "gqa_long": dict(B=1, H=64, Hkv=8, Sq=32768, Sk=32768, d=128, causal=True,
+                     dtype="bf16", seed=2, amp=0.5),
+    # split-K decode, one query row per head
+    "decode_splitk": dict(B=16, H=32, Hkv=8, Sq=1, Sk=65536, d=128, nsplit=32,
+                          causal=False, dtype="bf16", seed=3, amp=1.0),
+    # block-sparse: sliding window of 8 tiles, diagonal, 10% random lower tiles
+    "block_sparse": dict(B=2, H=16, Hkv=16, Sq=16384, Sk=16384, d=64, causal=False,
+                         dtype="bf16", seed=4, amp=1.0, tile=128, window=8, frac=0.1),
+}
+
+#: Row-softmax shapes (rows, cols): one row fits a CTA; one row spans a cluster.
+SOFTMAX_WORKLOADS = {
+    "rows_64k": dict(rows=16384, cols=16384, seed=5),
+    "rows_1m": dict(rows=1024, cols=262144, seed=6),
+}
+
+TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def default_scale(d):
+    """1/sqrt(d), the scale used by every workload."""
+    return 1.0 / math.sqrt(d)
+
+
+def make_qkv(B, H, Hkv, Sq, Sk, d, seed, dtype="bf16", amp=1.0, dv=None):
+    """Q [B,H,Sq,d], K [B,Hkv,Sk,d], V [B,Hkv,Sk,dv] on the CPU, contiguous."""
+    g = torch.Generator().manual_seed(seed)
+    dv = d if dv is None else dv
+    td = TORCH_DTYPES[dtype]
+    q = (torch.randn(B, H, Sq, d, generator=g) * amp).to(td)
+    k = (torch.randn(B, Hkv, Sk, d, generator=g) * amp).to(td)
+    v = (torch.randn(B, Hkv, Sk, dv, generator=g) * amp).to(td)
+    return q, k, v
+
+
+def make_rows(rows, cols, seed, dtype="f32", amp=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(rows, cols, generator=g) * amp).to(TORCH_DTYPES[dtype])
+
+
+def n_tiles(S, tile=128):
+    return -(-S // tile)
+
+
+def window_random_tile_mask(nqt, window=8, frac=0.1, seed=4):
+    """bool [nqt, nqt]: sliding window, diagonal, and random lower tiles.
+
+    Tile (i, j) is in the window when 0 <= i - j <= window - 1 (the diagonal
+    is part of it). Of the strictly-lower tiles outside the window, listed in
+    row-major order, round(frac * count) are drawn uniformly without
+    replacement by ``numpy.random.default_rng(seed).choice``.
+    """
+    i = np.arange(nqt)[:, None]
+    j = np.arange(nqt)[None, :]
+    mask = (i - j >= 0) & (i - j <= window - 1)
+    rest = np.argwhere(i - j >= window)          # row-major order
+    k = int(round(frac * len(rest)))
+    if k:
+        pick = np.random.default_rng(seed).choice(len(rest), k, replace=False)
+        sel = rest[pick]
+        mask[sel[:, 0], sel[:, 1]] = True
+    return mask
+
+
+def random_tile_mask(nqt, nkt, density, seed, nheads=None):
+    """bool [nqt, nkt] (or [nheads, nqt, nkt]) with each tile present w.p. density."""
+    rng = np.random.default_rng(seed)
+    shape = (nqt, nkt) if nheads is None else (nheads, nqt, nkt)
+    return rng.random(shape) < density
+
+
+def workload_inputs(name):
+    """(q, k, v, scale, extras) for a named workload, drawn on the CPU."""
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w["B"], w["H"], w["Hkv"], w["Sq"], w["Sk"], w["d"], w["seed"],
+                       w["dtype"], w["amp"])
+    extras = {}
+    if name == "block_sparse":
+        nqt = n_tiles(w["Sq"], w["tile"])
+        extras["tile_mask"] = window_random_tile_mask(nqt, w["window"], w["frac"], w["seed"])
+    return q, k, v, default_scale(w["d"]), extras

@@ -1,0 +1,39 @@
+"""Float64 CPU oracle for the fused online-softmax attention path.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product package
+``online_softmax_attention_rf_gb300`` imports this package, and the product
+never falls back to it. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import it.
+
+The oracle shares no code with the CUDA path: no kernels, headers, constant
+tables, tiling or pre-/post-processing. It computes the plain definition of
+each operation with NumPy in float64, three unfused passes per row, written
+so that it can be checked against the pages by eye.
+
+Modules
+-------
+``three_pass``   three-pass safe-softmax attention, row softmax, split-K
+                 partials and their log-sum-exp merge, the set of tiles that
+                 hold at least one visible (query, key) pair, and the
+                 block-sparse row lists of a tile mask.
+``incremental``  an independent float64 run of the incremental (online) form,
+                 used only to check that the derivation the GPU follows
+                 reaches the three-pass result.
+
+Every function here is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_pins.py`` against brute force, closed forms, invariants
+and library routines; none is "parity unpinned".
+"""
+
+from .three_pass import (  # noqa: F401
+    NEG_INF,
+    attention,
+    bsr_from_tile_mask,
+    decode_partials,
+    merge_partials,
+    softmax_rows,
+    split_bounds,
+    visible_mask,
+    visited_tiles,
+)
+from .incremental import incremental_attention  # noqa: F401
