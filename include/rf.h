@@ -1,0 +1,211 @@
+/*
+ * rf.h -- C ABI of librf.so: fused online-softmax attention for one GB300.
+ *
+ * The library computes the cascaded reduction behind safe-softmax attention
+ * -- row maximum, then the sum of exp(s - max), then the normalised P.V, with
+ * s = scale * Q K^T -- in one pass over K and V, keeping a running maximum,
+ * a running sum and an output accumulator on chip and rescaling them by
+ * exp(m_old - m_new) at every key tile. Scores are never written to memory.
+ *
+ * Sources (page title, section):
+ *  - RedFuser: An Automatic Operator Fusion Framework for Cascaded Reductions
+ *    on AI Accelerators -- technical summary section 1 (attention is a safe
+ *    softmax followed by a GEMM, a cascade of reductions), section 2 (formal
+ *    definition d_i = (+) F_i(X[l], D_i); feasibility: decomposable F_i,
+ *    commutative monoid, distributivity; incremental form with O(1) state),
+ *    section 3 (single-segment strategy in one CTA; multi-segment strategy
+ *    that partitions the input and merges partial results; FlashAttention
+ *    and FlashDecoding are special cases).
+ *  - Riepilogo Tecnico: FLASHLIGHT -- Metodologia items 2-4 (the max of the
+ *    softmax fused into Q K^T, the online softmax by rescaling with
+ *    e^(x-y) = e^x / e^y, small dimensions eliminated by tiling).
+ *  - Accelerating Sparse Transformer Inference on GPU (STOF) -- Méthodologie,
+ *    unified MHA module (row-compressed lists of block-sparse outer tiles;
+ *    masked tiles skipped entirely rather than zeroed after the fact).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    allocates no device memory, never synchronises (except rf_device_status),
+ *    and enqueues its kernels on the given stream; calls return at enqueue.
+ *  - Layouts are dense row-major, last dimension contiguous:
+ *      q, o : [B, H,   Sq, d]      k, v : [B, Hkv, Sk, d]      lse : [B, H, Sq]
+ *  - Query head h reads key/value head h / (H / Hkv) (grouped-query heads).
+ *  - Causal masking is bottom-right aligned: row i sees key j iff
+ *    j <= i + (Sk - Sq).
+ *  - lse is the natural-log log-sum-exp of the scaled, masked scores of a row.
+ *    A row that sees no key gets O = 0 and lse = -inf.
+ *  - Every call returns an rf_status. Invalid arguments are detected on the
+ *    host and no kernel is launched; rf_last_error() then describes the
+ *    problem (thread-local string, valid until the next call on the thread).
+ *  - Data-dependent faults found on the device (a block list that is out of
+ *    range or not ascending; a pipeline wait that ran out of time) never trap:
+ *    the kernel records a code in a device status word and skips the work.
+ *    rf_device_status() reads and clears it.
+ */
+#ifndef RF_H_
+#define RF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *rf_stream;
+
+typedef enum {
+  RF_OK = 0,
+  RF_ERR_INVALID = 1,      /* bad argument (host) or malformed block list (device) */
+  RF_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head dim outside {64,128} for bf16) */
+  RF_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  RF_ERR_TIMEOUT = 4       /* a device-side wait gave up (recorded in the device status word) */
+} rf_status;
+
+typedef enum {
+  RF_F32 = 0,   /* float32 in, float32 out, float32 arithmetic */
+  RF_BF16 = 1   /* bfloat16 in and out, float32 accumulation */
+} rf_dtype;
+
+/*
+ * Block-sparse tile lists (STOF's outer-tile row-compressed format).
+ * Tiles are 128 x 128 (query tile i covers rows [128 i, 128 i + 128), key
+ * tile j covers keys [128 j, 128 j + 128)). For query tile i of head n the
+ * listed key tiles are col_idx[row_ptr[n * nqt + i] .. row_ptr[n * nqt + i + 1]),
+ * in strictly ascending order, each in [0, nkt). Unlisted tiles are skipped
+ * entirely; listed tiles are attended in full (and, with causal, under the
+ * causal element mask).
+ *  per_head = 0: one list set shared by every (b, h); row_ptr has nqt + 1 entries.
+ *  per_head = 1: B*H list sets back to back, head n = b * H + h;
+ *                row_ptr has B*H*nqt + 1 entries.
+ * row_ptr and col_idx are device pointers (int32) owned by the caller; the
+ * struct itself is read on the host during the call only.
+ */
+typedef struct {
+  int tile_q;              /* must be 128 */
+  int tile_k;              /* must be 128 */
+  int nqt;                 /* must be ceil(Sq / 128) */
+  int nkt;                 /* must be ceil(Sk / 128) */
+  const int32_t *row_ptr;  /* device */
+  const int32_t *col_idx;  /* device */
+  int per_head;            /* 0 or 1 */
+} rf_blockmask;
+
+/*
+ * Row softmax: y[r, :] = exp(x[r, :] - max) / sum(exp(x[r, :] - max)).
+ * The pure two-reduction cascade of the RedFuser page's problem statement
+ * (maximum, then sum of exponentials), single pass over x: a row that fits
+ * one CTA (cols <= 32768 for f32) is held on chip between the reductions and
+ * the write; longer rows are split over a thread-block cluster that
+ * exchanges (max, sum) pairs through distributed shared memory
+ * (multi-segment strategy) and, beyond 8 x 32768 columns, re-read once.
+ *  x, y : [rows, cols] row-major, dtype dt (RF_F32 or RF_BF16); may alias.
+ *  rows >= 0, cols >= 0 (either 0: nothing is launched, RF_OK).
+ * A row whose entries are all -inf yields zeros. Errors: RF_ERR_INVALID for
+ * NULL pointers with nonzero sizes or negative sizes.
+ */
+rf_status rf_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
+                          rf_dtype dt, rf_stream stream);
+
+/*
+ * Attention forward (prefill), single-segment incremental form per query tile.
+ *  q [B,H,Sq,d], k/v [B,Hkv,Sk,d] (dtype dt), o [B,H,Sq,d] (dtype dt),
+ *  lse [B,H,Sq] float32 (may be NULL: not written).
+ *  scale > 0 and finite (scores are scale * q.k).
+ *  causal: 0 or 1.  blockmask: NULL for dense, else tile lists as above.
+ * Supported: RF_BF16 with d in {64, 128} (tensor-core kernel: TMA-staged K/V
+ * tiles, tcgen05 MMAs into tensor memory); RF_F32 with d % 4 == 0 and
+ * d <= 256 (exact SIMT kernel, one warp per query row).
+ * Pointers must be 16-byte aligned. B, H, Hkv >= 1; H % Hkv == 0;
+ * Sq, Sk >= 0 (Sq == 0: nothing launched; Sk == 0: O = 0, lse = -inf).
+ * Errors: RF_ERR_INVALID (NULL/misaligned pointers, bad sizes, H % Hkv,
+ * scale <= 0, blockmask fields inconsistent with Sq/Sk); RF_ERR_UNSUPPORTED
+ * (dtype/d combination not listed above).
+ */
+rf_status rf_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int H, int Hkv, int Sq, int Sk, int d, float scale,
+                      int causal, const rf_blockmask *blockmask, rf_dtype dt,
+                      rf_stream stream);
+
+/*
+ * Split-K decode (multi-segment strategy; FlashDecoding as a special case).
+ * One query row per head: q [B,H,1,d], k/v [B,Hkv,Sk,d], o [B,H,1,d], all
+ * dtype dt (RF_BF16); lse [B,H,1] float32 (may be NULL). The keys are cut
+ * into nsplit contiguous splits of Sk / nsplit keys (the last split takes the
+ * remainder); each split's partial (O_s normalised within the split, lse_s)
+ * goes to the workspace, then rf_splitk_merge combines them on the same
+ * stream. Every query head of a key/value group shares one pass over K/V.
+ *  ws: device workspace of at least rf_decode_workspace_bytes(B,H,nsplit,d)
+ *      bytes, 16-byte aligned, owned by the caller; ws_bytes its size.
+ *      Layout: o_part float32 [B*H, nsplit, d] followed by lse_part float32
+ *      [B*H, nsplit].
+ *  1 <= nsplit <= Sk; d in {64, 128}; H % Hkv == 0; H / Hkv <= 16.
+ * Errors: RF_ERR_INVALID, RF_ERR_UNSUPPORTED (dt != RF_BF16 or d).
+ */
+rf_status rf_attn_decode_splitk(const void *q, const void *k, const void *v, void *o,
+                                float *lse, int B, int H, int Hkv, int Sk, int d,
+                                float scale, int nsplit, float *ws, size_t ws_bytes,
+                                rf_dtype dt, rf_stream stream);
+
+/* Bytes of workspace rf_attn_decode_splitk needs: 4 * B*H*nsplit*(d + 1),
+ * rounded up to 256. Returns 0 for non-positive arguments. */
+size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d);
+
+/*
+ * Log-sum-exp merge of split partials (multi-segment strategy, merge step):
+ *   LSE = log sum_s exp(lse_s),   O = sum_s exp(lse_s - LSE) * O_s.
+ *  o_part float32 [rows, nsplit, d], lse_part float32 [rows, nsplit] (device);
+ *  o [rows, d] of dtype out_dt; lse float32 [rows] (may be NULL).
+ * Partials with lse_s = -inf contribute nothing; a row whose partials are all
+ * -inf gets O = 0 and LSE = -inf. rows >= 0, nsplit >= 1, 1 <= d <= 1024.
+ */
+rf_status rf_splitk_merge(const float *o_part, const float *lse_part, void *o, float *lse,
+                          int64_t rows, int nsplit, int d, rf_dtype out_dt,
+                          rf_stream stream);
+
+/*
+ * Build block-sparse tile lists from a dense tile mask on the device.
+ *  dense: uint8 [nheads, nqt, nkt] (nonzero = tile present), device.
+ *  row_ptr: int32 [nheads*nqt + 1] (device, written): exclusive scan of the
+ *           per-row counts; row_ptr[nheads*nqt] = total nnz.
+ *  col_idx: int32 [col_cap] (device, written): column indices of each row in
+ *           ascending order. If nnz > col_cap, entries past col_cap are not
+ *           written (row_ptr still holds the true counts) and the device
+ *           status word records RF_ERR_INVALID.
+ * One list set per head, in the layout rf_blockmask expects (per_head = 1
+ * when nheads > 1). nheads, nqt, nkt >= 1; col_cap >= 0.
+ */
+rf_status rf_blockmask_build(const uint8_t *dense, int nheads, int nqt, int nkt,
+                             int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                             rf_stream stream);
+
+/*
+ * Test aid: when visited is non-NULL, every later rf_attn_fwd on this host
+ * thread sets visited[((b*H + h) * nqt + qt) * nkt + kt] = 1 for each
+ * 128 x 128 tile (qt, kt) whose scores it computes. The caller zeroes the
+ * uint8 buffer (device, >= B*H*nqt*nkt bytes; visited_len its size).
+ * NULL turns it off. The skip set is checked bit-exactly against the set of
+ * tiles holding at least one visible (query, key) pair.
+ */
+rf_status rf_debug_set_visited(uint8_t *visited, int64_t visited_len);
+
+/*
+ * Synchronises the stream, then reads and clears the device status word of
+ * the current device. *code receives the raw code (0 = nothing recorded).
+ * Returns RF_OK, RF_ERR_TIMEOUT (a wait gave up), RF_ERR_INVALID (a malformed
+ * device-side list), or RF_ERR_CUDA.
+ */
+rf_status rf_device_status(rf_stream stream, int *code);
+
+/* Thread-local description of the last error returned on this thread. */
+const char *rf_last_error(void);
+
+/* ABI version, currently 1. */
+int rf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RF_H_ */

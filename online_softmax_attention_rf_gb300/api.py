@@ -1,0 +1,237 @@
+"""Thin ctypes binding of librf.so (declared in include/rf.h).
+
+Argument marshalling only: each function checks that its torch tensors are
+CUDA, contiguous and of the right dtype, passes their data pointers, sizes
+and the current CUDA stream to the C entry point of the same name, and turns
+a non-OK status into ``RFError``. Every step of the computation runs in the
+library's kernels; nothing here computes, and there is no CPU fallback -- if
+the library is missing, every call raises.
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+RF_OK, RF_ERR_INVALID, RF_ERR_UNSUPPORTED, RF_ERR_CUDA, RF_ERR_TIMEOUT = range(5)
+RF_F32, RF_BF16 = 0, 1
+_STATUS_NAMES = {0: "RF_OK", 1: "RF_ERR_INVALID", 2: "RF_ERR_UNSUPPORTED", 3: "RF_ERR_CUDA",
+                 4: "RF_ERR_TIMEOUT"}
+TILE = 128
+
+
+class RFError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (_STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+class RFBlockMask(ctypes.Structure):
+    _fields_ = [("tile_q", ctypes.c_int), ("tile_k", ctypes.c_int), ("nqt", ctypes.c_int),
+                ("nkt", ctypes.c_int), ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p),
+                ("per_head", ctypes.c_int)]
+
+
+_LIB = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+# name: (restype, argtypes) -- mirrors include/rf.h
+SIGNATURES = {
+    "rf_softmax_rows": (_I, [_P, _P, _I64, _I64, _I, _P]),
+    "rf_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
+                         ctypes.POINTER(RFBlockMask), _I, _P]),
+    "rf_attn_decode_splitk": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I,
+                                   _P]),
+    "rf_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "rf_splitk_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P]),
+    "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
+    "rf_debug_set_visited": (_I, [_P, _I64]),
+    "rf_device_status": (_I, [_P, ctypes.POINTER(_I)]),
+    "rf_last_error": (ctypes.c_char_p, []),
+    "rf_version": (_I, []),
+}
+
+
+def library_path():
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded librf.so; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                "librf.so is not built (%s); run `python -m online_softmax_attention_rf_gb300.build`"
+                % path)
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(status):
+    if status != RF_OK:
+        raise RFError(status, lib().rf_last_error().decode(errors="replace"))
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dt(t):
+    if t.dtype == torch.float32:
+        return RF_F32
+    if t.dtype == torch.bfloat16:
+        return RF_BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t.dtype)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+class BlockMask:
+    """Block-sparse 128 x 128 tile lists resident on the device.
+
+    ``row_ptr`` int32 [nheads*nqt + 1] and ``col_idx`` int32 [capacity];
+    ``per_head`` is 1 when each (batch, head) has its own lists.
+    """
+
+    def __init__(self, row_ptr, col_idx, nqt, nkt, per_head):
+        self.row_ptr, self.col_idx = row_ptr, col_idx
+        self.nqt, self.nkt, self.per_head = nqt, nkt, per_head
+
+    def as_struct(self):
+        return RFBlockMask(TILE, TILE, self.nqt, self.nkt, self.row_ptr.data_ptr(),
+                           self.col_idx.data_ptr(), self.per_head)
+
+    @classmethod
+    def from_dense(cls, tile_mask, device="cuda"):
+        """Build the lists on the device from a bool/uint8 mask [nqt, nkt] or
+        [nheads, nqt, nkt] (rf_blockmask_build)."""
+        tm = torch.as_tensor(tile_mask)
+        per_head = 1 if tm.dim() == 3 else 0
+        if tm.dim() == 2:
+            tm = tm.unsqueeze(0)
+        nheads, nqt, nkt = tm.shape
+        dense = tm.to(device=device, dtype=torch.uint8).contiguous()
+        row_ptr = torch.empty(nheads * nqt + 1, dtype=torch.int32, device=device)
+        col_idx = torch.empty(max(1, nheads * nqt * nkt), dtype=torch.int32, device=device)
+        blockmask_build(dense, row_ptr, col_idx)
+        return cls(row_ptr, col_idx, nqt, nkt, per_head)
+
+
+def blockmask_build(dense_u8, row_ptr, col_idx):
+    """rf_blockmask_build on [nheads, nqt, nkt] uint8 -> row_ptr, col_idx (in place)."""
+    _cuda(dense_u8, row_ptr, col_idx)
+    nheads, nqt, nkt = dense_u8.shape
+    _check(lib().rf_blockmask_build(_ptr(dense_u8), nheads, nqt, nkt, _ptr(row_ptr),
+                                    _ptr(col_idx), col_idx.numel(), _stream()))
+
+
+def softmax_rows(x, out=None):
+    """rf_softmax_rows: softmax over the last dim of a 2-D float32/bf16 tensor."""
+    _cuda(x)
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, cols]")
+    y = torch.empty_like(x) if out is None else out
+    _cuda(y)
+    _check(lib().rf_softmax_rows(_ptr(x), _ptr(y), x.shape[0], x.shape[1], _dt(x), _stream()))
+    return y
+
+
+def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,
+             with_lse=True):
+    """rf_attn_fwd: q [B,H,Sq,d], k/v [B,Hkv,Sk,d] -> (o, lse or None)."""
+    _cuda(q, k, v)
+    B, H, Sq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None and with_lse:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    _cuda(o, lse)
+    bm = ctypes.byref(blockmask.as_struct()) if blockmask is not None else None
+    _check(lib().rf_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Sq, Sk, d,
+                             float(scale), 1 if causal else 0, bm, _dt(q), _stream()))
+    return o, lse
+
+
+def decode_workspace_bytes(B, H, nsplit, d):
+    return int(lib().rf_decode_workspace_bytes(B, H, nsplit, d))
+
+
+def attn_decode_splitk(q, k, v, nsplit, scale=None, workspace=None, out=None, lse=None):
+    """rf_attn_decode_splitk: q [B,H,1,d], k/v [B,Hkv,Sk,d] -> (o, lse)."""
+    _cuda(q, k, v)
+    B, H, Sq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nbytes = decode_workspace_bytes(B, H, nsplit, d)
+    if workspace is None:
+        workspace = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device=q.device)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    _cuda(workspace, o, lse)
+    _check(lib().rf_attn_decode_splitk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv,
+                                       Sk, d, float(scale), nsplit, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _dt(q),
+                                       _stream()))
+    return o, lse
+
+
+def splitk_merge(o_part, lse_part, out_dtype=torch.bfloat16):
+    """rf_splitk_merge: o_part [rows, nsplit, d] f32, lse_part [rows, nsplit] f32."""
+    _cuda(o_part, lse_part)
+    rows, nsplit, d = o_part.shape
+    o = torch.empty(rows, d, dtype=out_dtype, device=o_part.device)
+    lse = torch.empty(rows, dtype=torch.float32, device=o_part.device)
+    _check(lib().rf_splitk_merge(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), rows, nsplit,
+                                 d, RF_F32 if out_dtype == torch.float32 else RF_BF16, _stream()))
+    return o, lse
+
+
+def set_debug_visited(buf):
+    """Record visited tiles of later attn_fwd calls on this thread into a uint8
+    CUDA tensor (None turns it off)."""
+    if buf is None:
+        _check(lib().rf_debug_set_visited(None, 0))
+    else:
+        _cuda(buf)
+        _check(lib().rf_debug_set_visited(_ptr(buf), buf.numel()))
+
+
+def device_status():
+    """Synchronise the current stream; return the device status code (0 = none)
+    and clear it. Raises RFError for a nonzero code."""
+    code = ctypes.c_int(0)
+    st = lib().rf_device_status(_stream(), ctypes.byref(code))
+    if st != RF_OK:
+        raise RFError(st, lib().rf_last_error().decode(errors="replace"))
+    return code.value

@@ -1,0 +1,202 @@
+// attn_simt.cu -- exact float32 attention forward, one warp per query row.
+//
+// The same single-pass cascade as the tensor-core kernel (running max m,
+// running sum l and accumulator acc per row, rescaled by exp(m_old - m_new)
+// at each key tile; RedFuser, section 2, incremental computation; FLASHLIGHT,
+// Metodologia item 3), in plain float32 FFMA arithmetic so that float32
+// inputs keep float32 accuracy (no TF32 rounding anywhere).
+//
+// Shape of the kernel (STOF, Méthodologie, row-wise kernel): the query is
+// split by rows, one warp owns one row, the reductions are warp shuffles and
+// no inter-warp synchronisation enters the arithmetic. The eight warps of a
+// CTA share 32-key K/V sub-tiles staged in shared memory. Masked 128 x 128
+// tiles are skipped entirely: the CTA walks the same tile list (dense range,
+// causal range, or block-sparse row) the tensor-core kernel walks.
+#include "rf_device.cuh"
+
+namespace rf {
+namespace {
+
+constexpr int kRows = 8;       // query rows (warps) per CTA
+constexpr int kSub = 32;       // keys per staged sub-tile
+constexpr int kTile = 128;     // mask tile side
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// DCH = ceil(d / 32): output columns owned by each lane (lane + 32 t).
+template <int DCH>
+__global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArgs a) {
+  extern __shared__ float smem[];
+  const int d = a.d, dp = a.d + 1;
+  float* Ks = smem;                 // [kSub][d + 1] (padded: conflict-free column walk)
+  float* Vs = Ks + kSub * dp;       // [kSub][d]
+  float* Qs = Vs + kSub * d;        // [kRows][d]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nrb = (a.Sq + kRows - 1) / kRows;
+  const int rb = blockIdx.x % nrb;
+  const int bh = blockIdx.x / nrb;
+  const int b = bh / a.H, h = bh % a.H;
+  const int hk = h / (a.H / a.Hkv);
+  const int r0 = rb * kRows, r1 = min(a.Sq, r0 + kRows);
+  const int i = r0 + warp;
+  const bool row_ok = i < a.Sq;
+  const float* qg = static_cast<const float*>(a.q) + (int64_t(bh) * a.Sq + i) * d;
+  const float* kg = static_cast<const float*>(a.k) + int64_t(b * a.Hkv + hk) * a.Sk * d;
+  const float* vg = static_cast<const float*>(a.v) + int64_t(b * a.Hkv + hk) * a.Sk * d;
+
+  if (row_ok)
+    for (int c = lane; c < d; c += 32) Qs[warp * d + c] = qg[c];
+
+  // keys visible to the CTA's last row bound every tile it may touch
+  const int64_t shift = int64_t(a.Sk) - a.Sq;  // bottom-right causal alignment
+  const int64_t kend = a.causal ? min64(a.Sk, int64_t(r1) + shift) : a.Sk;
+  const int64_t row_kend = a.causal ? min64(a.Sk, int64_t(i) + 1 + shift) : a.Sk;
+  const int qt = r0 / kTile;
+  int beg = 0, end = 0;
+  const int32_t* cols = nullptr;
+  if (a.row_ptr != nullptr) {
+    const int32_t* rp = a.row_ptr + (a.per_head ? int64_t(bh) * a.nqt : 0) + qt;
+    beg = rp[0];
+    end = rp[1];
+    cols = a.col_idx;
+  } else {
+    end = kend > 0 ? static_cast<int>((kend + kTile - 1) / kTile) : 0;
+  }
+
+  float m = kNegInf, l = 0.f;
+  float acc[DCH];
+#pragma unroll
+  for (int t = 0; t < DCH; ++t) acc[t] = 0.f;
+
+  int prev = -1;
+  for (int n = beg; n < end; ++n) {
+    int kt = n;
+    if (cols != nullptr) {
+      kt = cols[n];
+      if (kt < 0 || kt >= a.nkt || kt <= prev) {  // malformed list: record and stop
+        if (threadIdx.x == 0) record_status(a.status, dev_code(kDevBadList, kKerAttnSimt, 1));
+        break;
+      }
+      prev = kt;
+    }
+    if (int64_t(kt) * kTile >= kend) break;  // beyond every causal row: ascending list ends
+    if (a.visited != nullptr && threadIdx.x == 0)
+      a.visited[(int64_t(bh) * a.nqt + qt) * a.nkt + kt] = 1;
+    for (int sub = 0; sub < kTile / kSub; ++sub) {
+      const int k0 = kt * kTile + sub * kSub;
+      if (k0 >= kend) break;
+      __syncthreads();  // the previous sub-tile is consumed
+      const int d4 = d / 4;
+      for (int e = threadIdx.x; e < kSub * d4; e += kRows * 32) {
+        const int r = e / d4, c = (e % d4) * 4;
+        const int key = k0 + r;
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+        if (key < a.Sk) {
+          kv = *reinterpret_cast<const float4*>(kg + int64_t(key) * d + c);
+          vv = *reinterpret_cast<const float4*>(vg + int64_t(key) * d + c);
+        }
+        float* kd = Ks + r * dp + c;
+        kd[0] = kv.x; kd[1] = kv.y; kd[2] = kv.z; kd[3] = kv.w;
+        *reinterpret_cast<float4*>(Vs + r * d + c) = vv;
+      }
+      __syncthreads();
+      if (!row_ok) continue;
+      // scores of this row against the 32 keys (lane j <-> key k0 + j)
+      const int key = k0 + lane;
+      float s = kNegInf;
+      if (key < row_kend) {
+        float dot = 0.f;
+        const float* qr = Qs + warp * d;
+        const float* kr = Ks + lane * dp;
+        for (int c = 0; c < d; ++c) dot = fmaf(qr[c], kr[c], dot);
+        s = dot * a.scale;
+      }
+      // online update: m' = max(m, max s); alpha = exp(m - m'); p = exp(s - m')
+      const float mn = fmaxf(m, warp_max(s));
+      if (mn == kNegInf) continue;  // nothing visible to this row yet
+      const float alpha = (m == kNegInf) ? 0.f : expf(m - mn);
+      const float p = (s == kNegInf) ? 0.f : expf(s - mn);
+      l = l * alpha + warp_sum(p);
+#pragma unroll
+      for (int t = 0; t < DCH; ++t) acc[t] *= alpha;
+      for (int j = 0; j < kSub; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p, j);
+#pragma unroll
+        for (int t = 0; t < DCH; ++t) {
+          const int c = lane + 32 * t;
+          if (c < d) acc[t] = fmaf(pj, Vs[j * d + c], acc[t]);
+        }
+      }
+      m = mn;
+    }
+  }
+  if (!row_ok) return;
+  float* og = static_cast<float*>(a.o) + (int64_t(bh) * a.Sq + i) * d;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int t = 0; t < DCH; ++t) {
+    const int c = lane + 32 * t;
+    if (c < d) og[c] = acc[t] * inv;
+  }
+  if (lane == 0 && a.lse != nullptr)
+    a.lse[int64_t(bh) * a.Sq + i] = l > 0.f ? m + logf(l) : kNegInf;
+}
+
+// O = 0 and lse = -inf everywhere (no keys at all).
+__global__ void attn_fill_empty(uint32_t* o_words, int64_t n_words, float* lse, int64_t nrows) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n_words; e += stride)
+    o_words[e] = 0u;
+  if (lse != nullptr)
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < nrows; e += stride)
+      lse[e] = kNegInf;
+}
+
+template <int DCH>
+cudaError_t launch_dch(const AttnArgs& a, cudaStream_t s) {
+  const size_t smem = size_t(kSub * (a.d + 1) + kSub * a.d + kRows * a.d) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(attn_simt_f32_kernel<DCH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t nrb = (a.Sq + kRows - 1) / kRows;
+  const int64_t grid = nrb * a.B * a.H;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  attn_simt_f32_kernel<DCH><<<static_cast<unsigned>(grid), kRows * 32, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_empty(const AttnArgs& a, size_t elem_bytes, cudaStream_t s) {
+  const int64_t rows = int64_t(a.B) * a.H * a.Sq;
+  const int64_t words = rows * a.d * static_cast<int64_t>(elem_bytes) / 4;
+  attn_fill_empty<<<1184, 256, 0, s>>>(static_cast<uint32_t*>(a.o), words, a.lse, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t s) {
+  if (a.Sk == 0) return launch_attn_empty(a, sizeof(float), s);
+  switch ((a.d + 31) / 32) {
+    case 1: return launch_dch<1>(a, s);
+    case 2: return launch_dch<2>(a, s);
+    case 3: return launch_dch<3>(a, s);
+    case 4: return launch_dch<4>(a, s);
+    case 5: return launch_dch<5>(a, s);
+    case 6: return launch_dch<6>(a, s);
+    case 7: return launch_dch<7>(a, s);
+    default: return launch_dch<8>(a, s);
+  }
+}
+
+}  // namespace rf

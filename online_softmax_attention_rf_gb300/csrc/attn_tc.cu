@@ -1,0 +1,553 @@
+// attn_tc.cu -- bf16 attention forward on the tcgen05 tensor cores.
+//
+// The cascaded reduction max -> sum exp -> normalised P.V of safe-softmax
+// attention, fused into one pass over K and V in the incremental form
+// (RedFuser: An Automatic Operator Fusion Framework for Cascaded Reductions
+// on AI Accelerators, section 2: O(1) on-chip state per row; section 3:
+// single-segment strategy, one CTA per query tile, FlashAttention as a special
+// case). The max is taken straight from the Q K^T accumulator (FLASHLIGHT,
+// Metodologia item 2), the running sum and accumulator are rescaled by
+// exp(m_old - m_new) (item 3), and the head dimension is one tile (item 4).
+// Masked 128 x 128 tiles are never visited (STOF, Méthodologie: block-sparse
+// outer tiles in row-compressed lists; skipped, not zeroed).
+//
+// CTA = two 128-row query tiles of one (batch, head), sharing one K/V stream.
+// Warp roles (320 threads):
+//   warps 0-3  softmax group 0 (query tile 0: thread r owns row r, TMEM lane r)
+//   warps 4-7  softmax group 1 (query tile 1)
+//   warp 8     TMA producer: Q tiles, then K/V tiles into a shared-memory ring
+//   warp 9     TMEM allocator and MMA issuer (one elected lane)
+// Tensor memory (512 columns): S0 | S1 (128 f32 columns each) | O0 | O1 (D each).
+// Shared memory: Q0, Q1, P0, P1 (bf16, 128-byte swizzled K-major) and the K/V
+// ring (each slot one 128 x D tile; V is read as an MN-major operand).
+//
+// Per key tile u of query tile t:
+//   MMA:     S_t = Q_t K_u^T                      (tcgen05.mma, f32 in TMEM)
+//   softmax: m' = max(m, rowmax S); p = exp2(S*c - m'); l = a*l + rowsum p;
+//            if the max grew by more than 2^8, O_t *= a = exp2(m - m') (in TMEM)
+//            else the stale max is kept (a = 1; exact, since l and O share it);
+//            P_t = bf16(p) into shared memory
+//   MMA:     O_t += P_t V_u
+// The MMA lane issues QK0(u), PV1(u'), QK1(u), PV0(u) (u' the previous key
+// tile), so the softmax of each group overlaps about two MMAs of the other.
+// Epilogue: O = O_t / l (bf16), LSE = (m + log2 l) ln 2.
+//
+// Every wait is bounded (RF_WAIT_LIMIT_NS); on expiry the kernel records a
+// status code, the other roles notice the abort flag, and the CTA unwinds,
+// waits for its own copies and MMAs, and frees its tensor memory.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "rf_device.cuh"
+
+namespace rf {
+
+cudaError_t launch_attn_empty(const AttnArgs& a, size_t elem_bytes, cudaStream_t s);
+
+namespace {
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 256x
+constexpr int kBM = 128;                   // query rows per tile
+constexpr int kBN = 128;                   // keys per tile
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr int kChunk = 16384;              // one 128-row x 64-column bf16 swizzle block
+
+template <int D>
+struct Layout {
+  static constexpr int kTileBytes = kBM * D * 2;  // one Q, K or V tile
+  static constexpr int kStages = (D == 128) ? 3 : 6;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffKV = kOffP + 2 * kBM * kBN * 2;
+  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemS = 0;        // S0 at 0, S1 at 128
+  static constexpr uint32_t kTmemO = 2 * kBN;  // O0 at 256, O1 at 256 + D
+};
+
+struct Bars {
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t q_full[2];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t mma_idle;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Key-tile list of one query tile: dense/causal range or a block-sparse row.
+struct TileList {
+  const int32_t* cols;  // nullptr: range [0, n)
+  int n;                // entries (after causal truncation and validation)
+  __device__ __forceinline__ int at(int i) const { return cols ? cols[i] : i; }
+};
+
+struct Params {
+  int B, H, Hkv, Sq, Sk;
+  float scale_log2;
+  int causal;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  int per_head, nqt, nkt, pairs;
+  __nv_bfloat16* o;
+  float* lse;
+  uint8_t* visited;
+  int* status;
+};
+
+// The list of query tile qt of head bh; every role computes it identically.
+// Block-sparse rows are truncated at the first entry that is out of range, not
+// strictly ascending, or beyond the last causally visible key.
+__device__ TileList tile_list(const Params& p, int bh, int qt, bool record) {
+  TileList L{nullptr, 0};
+  if (qt >= p.nqt) return L;
+  const int64_t q_end = min64(p.Sq, int64_t(qt + 1) * kBM);
+  const int64_t kend = p.causal ? min64(p.Sk, q_end + (int64_t(p.Sk) - p.Sq)) : p.Sk;
+  if (kend <= 0) return L;
+  const int ntiles = static_cast<int>((kend + kBN - 1) / kBN);
+  if (p.row_ptr == nullptr) {
+    L.n = ntiles;
+    return L;
+  }
+  const int32_t* rp = p.row_ptr + (p.per_head ? int64_t(bh) * p.nqt : 0) + qt;
+  const int beg = rp[0], end = rp[1];
+  L.cols = p.col_idx + beg;
+  int n = 0, prev = -1;
+  for (int i = beg; i < end; ++i) {
+    const int c = p.col_idx[i];
+    if (c < 0 || c >= p.nkt || c <= prev) {
+      if (record) record_status(p.status, dev_code(kDevBadList, kKerAttnTc, 1));
+      break;
+    }
+    if (c >= ntiles) break;
+    prev = c;
+    ++n;
+  }
+  if (end < beg && record) record_status(p.status, dev_code(kDevBadList, kKerAttnTc, 2));
+  L.n = n;
+  return L;
+}
+
+// Merge cursor over the union of two ascending lists.
+struct UnionIter {
+  TileList l0, l1;
+  int i0 = 0, i1 = 0;
+  __device__ __forceinline__ bool next(int& u, bool& need0, bool& need1) {
+    const int a = i0 < l0.n ? l0.at(i0) : 0x7fffffff;
+    const int b = i1 < l1.n ? l1.at(i1) : 0x7fffffff;
+    if (a == 0x7fffffff && b == 0x7fffffff) return false;
+    u = min(a, b);
+    need0 = (a == u);
+    need1 = (b == u);
+    i0 += need0;
+    i1 += need1;
+    return true;
+  }
+};
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tm_s, uint32_t q_s, uint32_t k_s) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+    mma_bf16(tm_s, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024), idesc,
+             kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tm_o, uint32_t p_s, uint32_t v_s,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 1);
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    const uint64_t a = sdesc_sw128(p_s + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024);
+    const uint64_t b = sdesc_sw128(v_s + kk * 16 * 128, kChunk, 1024);
+    mma_bf16(tm_o, a, b, idesc, (kk > 0 || accumulate) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using L = Layout<D>;
+  constexpr int NS = L::kStages;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars& bar = *reinterpret_cast<Bars*>(smem + L::kOffBar);
+  const uint32_t s_base = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // heavy query-tile pairs first (causal: later tiles see more keys)
+  const int BH = p.B * p.H;
+  const int pair = p.pairs - 1 - static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int b = bh / p.H, h = bh % p.H;
+  const int bk = b * p.Hkv + h / (p.H / p.Hkv);
+  const int qt0 = 2 * pair;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.kv_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar.q_full[t], 1);
+      mbar_init(&bar.s_full[t], 1);
+      mbar_init(&bar.s_free[t], 4);
+      mbar_init(&bar.p_full[t], 4);
+      mbar_init(&bar.o_done[t], 1);
+    }
+    mbar_init(&bar.mma_idle, 1);
+    bar.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&bar.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bar.tmem_base;
+  volatile int* abort_flag = &bar.abort_flag;
+
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      UnionIter it{tile_list(p, bh, qt0, false), tile_list(p, bh, qt0 + 1, false)};
+      const int bhq = bh;
+      for (int t = 0; t < 2; ++t) {
+        if ((t == 0 ? it.l0.n : it.l1.n) == 0) continue;
+        mbar_arrive_expect_tx(&bar.q_full[t], L::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + L::kOffQ + t * L::kTileBytes + c * kChunk, &tm_q, &bar.q_full[t],
+                      c * 64, (qt0 + t) * kBM, bhq);
+      }
+      int u;
+      bool n0, n1;
+      int seq = 0;
+      int last[8];
+      for (int i = 0; i < NS; ++i) last[i] = -1;
+      bool ok = true;
+      while (ok && it.next(u, n0, n1)) {
+        for (int kv = 0; kv < 2 && ok; ++kv, ++seq) {
+          const int slot = seq % NS;
+          ok = mbar_wait(&bar.kv_empty[slot], ((seq / NS) & 1) ^ 1, p.status,
+                         dev_code(kDevTimeout, kKerAttnTc, 10), abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar.kv_full[slot], L::kTileBytes);
+          unsigned char* dst = smem + L::kOffKV + slot * L::kTileBytes;
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(dst + c * kChunk, kv == 0 ? &tm_k : &tm_v, &bar.kv_full[slot], c * 64,
+                        u * kBN, bk);
+          last[slot] = seq;
+        }
+      }
+      // never leave with copies in flight
+      for (int i = 0; i < NS; ++i)
+        if (last[i] >= 0)
+          mbar_wait(&bar.kv_full[i], (last[i] / NS) & 1, p.status,
+                    dev_code(kDevTimeout, kKerAttnTc, 11), nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    // Issue order per key tile u (previous tile u'):
+    //   QK0(u), PV1(u'), QK1(u), PV0(u)
+    // so each softmax group has about two MMAs of slack between its S being
+    // ready and its P being consumed, and K/V slots are released as early as
+    // their last reader is issued (commit-tracked).
+    if (lane == 0) {
+      UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, false)};
+      const uint32_t q_s[2] = {s_base + L::kOffQ, s_base + L::kOffQ + L::kTileBytes};
+      const uint32_t p_s[2] = {s_base + L::kOffP, s_base + L::kOffP + kBM * kBN * 2};
+      const uint32_t tm_s[2] = {tmem + L::kTmemS, tmem + L::kTmemS + kBN};
+      const uint32_t tm_o[2] = {tmem + L::kTmemO, tmem + L::kTmemO + D};
+      int nq[2] = {0, 0};    // QK tiles issued per query tile
+      int npv[2] = {0, 0};   // PV tiles issued per query tile
+      bool q_ready[2] = {false, false};
+      bool issued_any = false;
+      int pend1 = -1;        // load sequence number of the V tile query tile 1 still owes
+      int seq = 0;
+      bool ok = true;
+      auto wait = [&](uint64_t* bb, int parity, int site) {
+        return mbar_wait(bb, parity, p.status, dev_code(kDevTimeout, kKerAttnTc, site), abort_flag);
+      };
+      auto slot_addr = [&](int sq) { return s_base + L::kOffKV + (sq % NS) * L::kTileBytes; };
+      auto qk = [&](int t, int kseq, int u) -> bool {
+        if (!q_ready[t]) {
+          if (!wait(&bar.q_full[t], 0, 22)) return false;
+          q_ready[t] = true;
+        }
+        if (nq[t] > 0) {
+          if (!wait(&bar.s_free[t], (nq[t] - 1) & 1, 23)) return false;
+          tc_fence_after_sync();
+        }
+        issue_qk<D>(tm_s[t], q_s[t], slot_addr(kseq));
+        mma_commit(&bar.s_full[t]);
+        issued_any = true;
+        ++nq[t];
+        if (p.visited != nullptr) p.visited[(int64_t(bh) * p.nqt + qt0 + t) * p.nkt + u] = 1;
+        return true;
+      };
+      auto pv = [&](int t, int vseq) -> bool {
+        if (!wait(&bar.kv_full[vseq % NS], (vseq / NS) & 1, 24)) return false;
+        if (!wait(&bar.p_full[t], npv[t] & 1, 25)) return false;
+        tc_fence_after_sync();
+        issue_pv<D>(tm_o[t], p_s[t], slot_addr(vseq), npv[t] > 0);
+        mma_commit(&bar.o_done[t]);
+        ++npv[t];
+        return true;
+      };
+      int u;
+      bool need0, need1;
+      while (ok && it.next(u, need0, need1)) {
+        const int kseq = seq, vseq = seq + 1;
+        seq += 2;
+        ok = wait(&bar.kv_full[kseq % NS], (kseq / NS) & 1, 21);
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (need0 && !(ok = qk(0, kseq, u))) break;
+        if (pend1 >= 0) {
+          if (!(ok = pv(1, pend1))) break;
+          mma_commit(&bar.kv_empty[pend1 % NS]);
+          pend1 = -1;
+        }
+        if (need1 && !(ok = qk(1, kseq, u))) break;
+        mma_commit(&bar.kv_empty[kseq % NS]);
+        if (need0 && !(ok = pv(0, vseq))) break;
+        if (need1)
+          pend1 = vseq;
+        else
+          mma_commit(&bar.kv_empty[vseq % NS]);
+      }
+      if (ok && pend1 >= 0 && (ok = pv(1, pend1))) mma_commit(&bar.kv_empty[pend1 % NS]);
+      // never leave with MMAs in flight (their operands live in this CTA)
+      if (issued_any) {
+        mma_commit(&bar.mma_idle);
+        mbar_wait(&bar.mma_idle, 0, p.status, dev_code(kDevTimeout, kKerAttnTc, 28), nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax groups
+    const int t = warp >> 2;             // query tile of this group
+    const int r = threadIdx.x & 127;     // row within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int qt = qt0 + t;
+    const int64_t row = int64_t(qt) * kBM + r;
+    const TileList list = tile_list(p, bh, qt, false);
+    const uint32_t tm_s = tmem + L::kTmemS + t * kBN + lane_off;
+    const uint32_t tm_o = tmem + L::kTmemO + t * D + lane_off;
+    unsigned char* p_tile = smem + L::kOffP + t * (kBM * kBN * 2);
+    const int64_t shift = int64_t(p.Sk) - p.Sq;
+    const int64_t row_lim = p.causal ? min64(p.Sk, row + 1 + shift) : p.Sk;
+    const int64_t tile_first_lim =
+        p.causal ? min64(p.Sk, int64_t(qt) * kBM + 1 + shift) : p.Sk;
+    float m_run = kNegInf, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < list.n && ok; ++j) {
+      const int u = list.at(j);
+      ok = mbar_wait_warp(&bar.s_full[t], j & 1, p.status, dev_code(kDevTimeout, kKerAttnTc, 30),
+                          abort_flag);
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t sr[128];
+      tmem_ld64_wait(tm_s, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
+      tmem_ld64_wait(tm_s + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.s_free[t]);
+      // element mask only where the tile crosses the causal diagonal or Sk
+      const int64_t k0 = int64_t(u) * kBN;
+      float mx = kNegInf;
+      if (k0 + kBN > tile_first_lim) {
+        const int64_t lim = row_lim - k0;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          if (c >= lim) sr[c] = __float_as_uint(kNegInf);
+          mx = fmaxf(mx, __uint_as_float(sr[c]));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      }
+      const float m_new = (mx == kNegInf) ? m_run : fmaxf(m_run, mx * p.scale_log2);
+      const bool resc = m_new > m_run + kRescaleThreshold;
+      const float m_use = resc ? m_new : m_run;
+      const float alpha = resc ? ex2_approx(m_run - m_new) : 1.f;
+      const float sh = (m_use == kNegInf) ? 0.f : m_use;
+      float sum = 0.f;
+      uint32_t pw[64];
+#pragma unroll
+      for (int c = 0; c < kBN; c += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), p.scale_log2, -sh));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -sh));
+        sum += p0 + p1;
+        pw[c >> 1] = pack_bf16x2(p0, p1);
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_use;
+      if (j > 0) {
+        // the previous P.V must be done: P_t is free and O_t holds its sum
+        ok = mbar_wait_warp(&bar.o_done[t], (j - 1) & 1, p.status,
+                            dev_code(kDevTimeout, kKerAttnTc, 31), abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            tmem_ld32_wait(tm_o + c, ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32_wait(tm_o + c, ov);
+          }
+        }
+      }
+      // P (bf16) into the 128-byte-swizzled K-major tile: 16-byte piece q of
+      // row r sits at r*128 + ((q ^ (r & 7)) * 16) inside its 64-key block
+#pragma unroll
+      for (int q16 = 0; q16 < 16; ++q16) {
+        const int blk = q16 >> 3, piece = q16 & 7;
+        uint4* dst = reinterpret_cast<uint4*>(p_tile + blk * kChunk + r * 128 +
+                                              ((piece ^ (r & 7)) << 4));
+        *dst = make_uint4(pw[4 * q16], pw[4 * q16 + 1], pw[4 * q16 + 2], pw[4 * q16 + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.p_full[t]);
+    }
+    // epilogue: O = acc / l, LSE = (m + log2 l) ln 2
+    const bool row_ok = row < p.Sq && qt < p.nqt;
+    __nv_bfloat16* og = p.o + (int64_t(bh) * p.Sq + row) * D;
+    if (ok && list.n > 0) {
+      ok = mbar_wait_warp(&bar.o_done[t], (list.n - 1) & 1, p.status,
+                          dev_code(kDevTimeout, kKerAttnTc, 32), abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32_wait(tm_o + c, ov);
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(ov[e + 4]) * inv, __uint_as_float(ov[e + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(ov[e + 6]) * inv, __uint_as_float(ov[e + 7]) * inv);
+              *reinterpret_cast<uint4*>(og + c + e) = w;
+            }
+          }
+        }
+        if (row_ok && p.lse != nullptr)
+          p.lse[int64_t(bh) * p.Sq + row] =
+              l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : kNegInf;
+      }
+    } else if (ok && row_ok) {
+      // no visible key for any row of this tile
+      for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(og + c) = make_uint4(0, 0, 0, 0);
+      if (p.lse != nullptr) p.lse[int64_t(bh) * p.Sq + row] = kNegInf;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [BH, S, D] bf16, 128-byte swizzle, boxes of 64 columns x 128 rows.
+bool make_map(CUtensorMap* m, const void* base, int D, int S, int BH) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(S) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, D, a.Sq, a.B * a.H) || !make_map(&mk, a.k, D, a.Sk, a.B * a.Hkv) ||
+      !make_map(&mv, a.v, D, a.Sk, a.B * a.Hkv)) {
+    *why = "tensor map encoding failed";
+    return cudaErrorInvalidValue;
+  }
+  constexpr int smem = Layout<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) {
+    *why = "shared memory attribute";
+    return e;
+  }
+  Params p{};
+  p.B = a.B; p.H = a.H; p.Hkv = a.Hkv; p.Sq = a.Sq; p.Sk = a.Sk;
+  p.scale_log2 = a.scale * kLog2e;
+  p.causal = a.causal;
+  p.row_ptr = a.row_ptr; p.col_idx = a.col_idx; p.per_head = a.per_head;
+  p.nqt = a.nqt; p.nkt = a.nkt;
+  p.pairs = (a.nqt + 1) / 2;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.visited = a.visited;
+  p.status = a.status;
+  const int64_t grid = int64_t(p.pairs) * a.B * a.H;
+  if (grid > 0x7fffffffLL) {
+    *why = "grid too large";
+    return cudaErrorInvalidConfiguration;
+  }
+  attn_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc_bf16(const AttnArgs& a, cudaStream_t s, const char** why) {
+  if (a.Sk == 0) return launch_attn_empty(a, 2, s);
+  if (a.d == 128) return launch_d<128>(a, s, why);
+  return launch_d<64>(a, s, why);
+}
+
+}  // namespace rf

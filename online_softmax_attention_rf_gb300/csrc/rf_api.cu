@@ -1,0 +1,273 @@
+// rf_api.cu -- the C ABI of librf.so: argument validation, dispatch to the
+// kernel launchers, error strings and the device status word.
+//
+// Every entry point checks its arguments on the host before touching CUDA;
+// an invalid call launches nothing and returns RF_ERR_INVALID with a
+// thread-local message (rf_last_error). No entry point allocates device
+// memory or synchronises, except rf_device_status which exists to do so.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+
+#include "rf_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = {0};
+thread_local uint8_t* g_visited = nullptr;
+thread_local int64_t g_visited_len = 0;
+
+// The device status word (one per device that loads the library).
+__device__ int g_status_word = 0;
+std::atomic<int*> g_status_ptr[128];
+
+rf_status fail(rf_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+rf_status ok() {
+  g_err[0] = 0;
+  return RF_OK;
+}
+
+rf_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RF_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+namespace rf {
+
+int* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (dev >= 0 && dev < 128) {
+    int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (p != nullptr) return p;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  if (dev >= 0 && dev < 128) g_status_ptr[dev].store(static_cast<int*>(p), std::memory_order_release);
+  return static_cast<int*>(p);
+}
+
+uint8_t* debug_visited(int64_t* len) {
+  if (len != nullptr) *len = g_visited_len;
+  return g_visited;
+}
+
+}  // namespace rf
+
+extern "C" {
+
+const char* rf_last_error(void) { return g_err; }
+
+int rf_version(void) { return 1; }
+
+rf_status rf_debug_set_visited(uint8_t* visited, int64_t visited_len) {
+  if (visited != nullptr && visited_len <= 0)
+    return fail(RF_ERR_INVALID, "rf_debug_set_visited: visited_len must be > 0");
+  g_visited = visited;
+  g_visited_len = visited ? visited_len : 0;
+  return ok();
+}
+
+rf_status rf_device_status(rf_stream stream, int* code) {
+  if (code == nullptr) return fail(RF_ERR_INVALID, "rf_device_status: code is NULL");
+  *code = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_device_status: stream synchronize");
+  int* w = rf::status_word();
+  if (w == nullptr) return fail(RF_ERR_CUDA, "rf_device_status: no device status word");
+  int v = 0;
+  e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_device_status: read");
+  const int zero = 0;
+  e = cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_device_status: clear");
+  *code = v;
+  if (v == 0) return ok();
+  const int kind = v >> 16;
+  if (kind == rf::kDevTimeout)
+    return fail(RF_ERR_TIMEOUT, "device wait gave up (code 0x%x)", v);
+  return fail(RF_ERR_INVALID, "device detected invalid data (code 0x%x)", v);
+}
+
+rf_status rf_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols, rf_dtype dt,
+                          rf_stream stream) {
+  if (rows < 0 || cols < 0) return fail(RF_ERR_INVALID, "rf_softmax_rows: negative size");
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_softmax_rows: bad dtype");
+  if (rows == 0 || cols == 0) return ok();
+  if (x == nullptr || y == nullptr) return fail(RF_ERR_INVALID, "rf_softmax_rows: NULL pointer");
+  if (rows > INT32_MAX) return fail(RF_ERR_INVALID, "rf_softmax_rows: rows > 2^31-1");
+  if (cols > (int64_t(1) << 40)) return fail(RF_ERR_INVALID, "rf_softmax_rows: cols too large");
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_softmax_rows: no CUDA device");
+  cudaError_t e = rf::launch_softmax_rows(x, y, rows, cols, dt,
+                                          reinterpret_cast<cudaStream_t>(stream), st);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_softmax_rows: launch");
+  return ok();
+}
+
+rf_status rf_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                      const rf_blockmask* bm, rf_dtype dt, rf_stream stream) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sq < 0 || Sk < 0 || d < 1)
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: bad sizes B=%d H=%d Hkv=%d Sq=%d Sk=%d d=%d", B, H,
+                Hkv, Sq, Sk, d);
+  if (H % Hkv != 0) return fail(RF_ERR_INVALID, "rf_attn_fwd: H %% Hkv != 0");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(RF_ERR_INVALID, "rf_attn_fwd: causal must be 0/1");
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_attn_fwd: bad dtype");
+  if (dt == RF_BF16 && d != 64 && d != 128)
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: bf16 supports d in {64,128}, got %d", d);
+  if (dt == RF_F32 && (d % 4 != 0 || d > 256))
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: f32 supports d %% 4 == 0, d <= 256");
+  const int64_t esz = dt == RF_F32 ? 4 : 2;
+  if (int64_t(B) * H * Sq * d * esz > (int64_t(1) << 46) ||
+      int64_t(B) * Hkv * Sk * d * esz > (int64_t(1) << 46))
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: tensors too large");
+  const int nqt = static_cast<int>(cdiv(Sq, 128)), nkt = static_cast<int>(cdiv(Sk, 128));
+  if (bm != nullptr) {
+    if (bm->tile_q != 128 || bm->tile_k != 128)
+      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask tiles must be 128x128");
+    if (bm->nqt != nqt || bm->nkt != nkt)
+      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask nqt/nkt (%d,%d) != (%d,%d)", bm->nqt,
+                  bm->nkt, nqt, nkt);
+    if (bm->per_head != 0 && bm->per_head != 1)
+      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask per_head must be 0/1");
+    if (Sq > 0 && Sk > 0 && (bm->row_ptr == nullptr || bm->col_idx == nullptr))
+      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask lists are NULL");
+  }
+  if (Sq == 0) return ok();
+  if (q == nullptr || o == nullptr || (Sk > 0 && (k == nullptr || v == nullptr)))
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: NULL tensor pointer");
+  if (!aligned(q, 16) || !aligned(o, 16) || (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))))
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: q/k/v/o must be 16-byte aligned");
+  if (lse != nullptr && !aligned(lse, 4))
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: lse must be 4-byte aligned");
+  int64_t vlen = 0;
+  uint8_t* visited = rf::debug_visited(&vlen);
+  if (visited != nullptr && vlen < int64_t(B) * H * nqt * nkt)
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: visited buffer too small");
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_attn_fwd: no CUDA device");
+
+  rf::AttnArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.Sq = Sq; a.Sk = Sk; a.d = d;
+  a.scale = scale; a.causal = causal;
+  a.row_ptr = bm ? bm->row_ptr : nullptr;
+  a.col_idx = bm ? bm->col_idx : nullptr;
+  a.per_head = bm ? bm->per_head : 0;
+  a.nqt = nqt; a.nkt = nkt;
+  a.visited = visited;
+  a.status = st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dt == RF_F32) {
+    e = rf::launch_attn_simt_f32(a, s);
+  } else {
+    const char* why = nullptr;
+    e = rf::launch_attn_tc_bf16(a, s, &why);
+    if (e != cudaSuccess && why != nullptr)
+      return fail(RF_ERR_CUDA, "rf_attn_fwd: %s: %s", why, cudaGetErrorString(e));
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "rf_attn_fwd: launch");
+  return ok();
+}
+
+size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d) {
+  if (B < 1 || H < 1 || nsplit < 1 || d < 1) return 0;
+  const size_t n = size_t(B) * H * nsplit * (size_t(d) + 1) * sizeof(float);
+  return (n + 255) / 256 * 256;
+}
+
+rf_status rf_attn_decode_splitk(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int Hkv, int Sk, int d, float scale, int nsplit,
+                                float* ws, size_t ws_bytes, rf_dtype dt, rf_stream stream) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sk < 1 || d < 1)
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: bad sizes");
+  if (H % Hkv != 0) return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: H %% Hkv != 0");
+  if (H / Hkv > 16) return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitk: H/Hkv > 16");
+  if (nsplit < 1 || nsplit > Sk)
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: need 1 <= nsplit <= Sk");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: scale must be finite and > 0");
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: dtype");
+  if (dt != RF_BF16 || (d != 64 && d != 128))
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitk: bf16 with d in {64,128} only");
+  if (int64_t(B) * Hkv * Sk * d * 2 > (int64_t(1) << 46))
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: tensors too large");
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || ws == nullptr)
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: NULL pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(ws, 16))
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: pointers must be 16-byte aligned");
+  if (lse != nullptr && !aligned(lse, 4))
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: lse must be 4-byte aligned");
+  if (ws_bytes < rf_decode_workspace_bytes(B, H, nsplit, d))
+    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: workspace too small (%zu < %zu)",
+                ws_bytes, rf_decode_workspace_bytes(B, H, nsplit, d));
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_attn_decode_splitk: no CUDA device");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* o_part = ws;
+  float* lse_part = ws + size_t(B) * H * nsplit * d;
+  cudaError_t e = rf::launch_decode_partials(q, k, v, o_part, lse_part, B, H, Hkv, Sk, d, scale,
+                                             nsplit, s, st);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_attn_decode_splitk: partials launch");
+  e = rf::launch_splitk_merge(o_part, lse_part, o, lse, int64_t(B) * H, nsplit, d, dt, s);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_attn_decode_splitk: merge launch");
+  return ok();
+}
+
+rf_status rf_splitk_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                          int64_t rows, int nsplit, int d, rf_dtype out_dt, rf_stream stream) {
+  if (rows < 0 || nsplit < 1 || d < 1 || d > 1024)
+    return fail(RF_ERR_INVALID, "rf_splitk_merge: bad sizes");
+  if (out_dt != RF_F32 && out_dt != RF_BF16)
+    return fail(RF_ERR_INVALID, "rf_splitk_merge: bad dtype");
+  if (rows == 0) return ok();
+  if (rows > INT32_MAX) return fail(RF_ERR_INVALID, "rf_splitk_merge: rows > 2^31-1");
+  if (o_part == nullptr || lse_part == nullptr || o == nullptr)
+    return fail(RF_ERR_INVALID, "rf_splitk_merge: NULL pointer");
+  if (!aligned(o_part, 4) || !aligned(lse_part, 4) || !aligned(o, out_dt == RF_F32 ? 4 : 2) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return fail(RF_ERR_INVALID, "rf_splitk_merge: misaligned pointer");
+  cudaError_t e = rf::launch_splitk_merge(o_part, lse_part, o, lse, rows, nsplit, d, out_dt,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_splitk_merge: launch");
+  return ok();
+}
+
+rf_status rf_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt, int32_t* row_ptr,
+                             int32_t* col_idx, int64_t col_cap, rf_stream stream) {
+  if (nheads < 1 || nqt < 1 || nkt < 1 || col_cap < 0)
+    return fail(RF_ERR_INVALID, "rf_blockmask_build: bad sizes");
+  if (int64_t(nheads) * nqt * nkt > INT32_MAX)
+    return fail(RF_ERR_INVALID, "rf_blockmask_build: mask larger than 2^31-1 tiles");
+  if (dense == nullptr || row_ptr == nullptr || (col_cap > 0 && col_idx == nullptr))
+    return fail(RF_ERR_INVALID, "rf_blockmask_build: NULL pointer");
+  if (!aligned(row_ptr, 4) || (col_idx != nullptr && !aligned(col_idx, 4)))
+    return fail(RF_ERR_INVALID, "rf_blockmask_build: misaligned output");
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_blockmask_build: no CUDA device");
+  cudaError_t e = rf::launch_blockmask_build(dense, nheads, nqt, nkt, row_ptr, col_idx, col_cap,
+                                             reinterpret_cast<cudaStream_t>(stream), st);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_blockmask_build: launch");
+  return ok();
+}
+
+}  // extern "C"

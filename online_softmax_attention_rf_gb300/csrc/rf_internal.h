@@ -1,0 +1,74 @@
+// rf_internal.h -- declarations shared by the host entry points and the
+// kernel translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "rf.h"
+
+// Upper bound on any single device-side wait (mbarrier phase, TMEM, peer).
+// Far above any legitimate wait in these kernels (microseconds), far below a
+// watchdog: a wait that exceeds it records a status code and unwinds.
+#define RF_WAIT_LIMIT_NS 2000000000ull
+
+namespace rf {
+
+// Device status word codes: (kind << 16) | (kernel << 8) | site.
+enum DevKind : int { kDevTimeout = 1, kDevBadList = 2, kDevCapacity = 3 };
+enum DevKernel : int {
+  kKerSoftmax = 1,
+  kKerAttnSimt = 2,
+  kKerAttnTc = 3,
+  kKerDecode = 4,
+  kKerMerge = 5,
+  kKerBlockmask = 6
+};
+
+__host__ __device__ constexpr int dev_code(int kind, int kernel, int site) {
+  return (kind << 16) | (kernel << 8) | site;
+}
+
+// Device address of the status word for the current device (nullptr on error).
+int* status_word();
+
+// Visited-tile debug buffer for the calling host thread (nullptr = off).
+uint8_t* debug_visited(int64_t* len);
+
+// Arguments of one attention-forward launch (validated on the host).
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, Hkv, Sq, Sk, d;
+  float scale;
+  int causal;
+  // block-sparse lists (row_ptr == nullptr: dense)
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  int per_head;
+  int nqt, nkt;
+  uint8_t* visited;  // optional debug output, [B*H*nqt*nkt]
+  int* status;
+};
+
+// Each launcher validates nothing (the entry points do) and returns the
+// launch error, if any.
+cudaError_t launch_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
+                                rf_dtype dt, cudaStream_t s, int* status);
+cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attn_tc_bf16(const AttnArgs& a, cudaStream_t s, const char** why);
+cudaError_t launch_decode_partials(const void* q, const void* k, const void* v, float* o_part,
+                                   float* lse_part, int B, int H, int Hkv, int Sk, int d,
+                                   float scale, int nsplit, cudaStream_t s, int* status);
+cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                                int64_t rows, int nsplit, int d, rf_dtype out_dt,
+                                cudaStream_t s);
+cudaError_t launch_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
+                                   int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
+                                   cudaStream_t s, int* status);
+
+}  // namespace rf

@@ -1,0 +1,318 @@
+// softmax_rows.cu -- row softmax, the pure two-reduction cascade.
+//
+// RedFuser (An Automatic Operator Fusion Framework for Cascaded Reductions
+// on AI Accelerators), technical summary section 1: softmax is a cascade of
+// reductions (maximum, then sum of exponentials) where each waits for the
+// root of the one before; section 2: fusing the chain means the input is
+// loaded once; section 3: single-segment (one CTA) and multi-segment
+// (partition, then merge the partial results) strategies.
+//
+// Shapes of the kernel:
+//  * on chip, one CTA per row (row <= kSliceBytes): the row is copied into
+//    shared memory once (cp.async.bulk, 16 KB pieces, each with its own
+//    mbarrier so the maximum starts on the first piece), then
+//    m = max, p = exp(x - m) written back in place with l = sum p, and
+//    y = p / l stored -- 1 read + 1 write of HBM per element;
+//  * on chip, one cluster of up to 8 CTAs per row (multi-segment): each CTA
+//    reduces its slice to (m_c, l_c), the pairs are exchanged through
+//    distributed shared memory and combined as L = sum_c l_c exp(m_c - M),
+//    and each CTA scales its slice by exp(m_c - M) / L -- still 1R + 1W;
+//  * streaming, one cluster of 8 per row, for rows longer than 8 slices: each
+//    thread folds its elements into a running (m, l) (the incremental form,
+//    O(1) state), the cluster combines, and a second read writes y (2R + 1W).
+// x and y may alias: every element is read before the thread that writes it
+// writes it.
+#include <cooperative_groups.h>
+
+#include "rf_device.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace rf {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSliceBytes = 128 * 1024;  // largest slice one CTA holds on chip
+constexpr int kPiece = 16384;            // bytes per bulk copy / mbarrier
+constexpr int kMaxPieces = kSliceBytes / kPiece;
+constexpr int kMaxCluster = 8;
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v) {
+  return static_cast<float>(v);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Block-wide reductions; `red` holds one float per warp.
+__device__ __forceinline__ float block_max(float x, float* red) {
+  x = warp_max(x);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = x;
+  __syncthreads();
+  const float r = (threadIdx.x & 31) < nw ? red[threadIdx.x & 31] : kNegInf;
+  return warp_max(r);
+}
+
+__device__ __forceinline__ float block_sum(float x, float* red) {
+  x = warp_sum(x);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = x;
+  __syncthreads();
+  const float r = (threadIdx.x & 31) < nw ? red[threadIdx.x & 31] : 0.f;
+  return warp_sum(r);
+}
+
+// exp(x - m) for a finite shift m; exp(-inf - m) = 0.
+__device__ __forceinline__ float exp_shift(float x, float m) { return ex2_approx((x - m) * kLog2e); }
+
+// Combine this CTA's (m, l) with the other CTAs of its cluster through
+// distributed shared memory; every thread gets the row's (M, L).
+__device__ __forceinline__ void cluster_combine(float m, float l, float2* pair, float& M, float& L) {
+  cg::cluster_group cl = cg::this_cluster();
+  const unsigned nc = cl.num_blocks();
+  if (threadIdx.x == 0) *pair = make_float2(m, l);
+  cl.sync();
+  M = kNegInf;
+  for (unsigned c = 0; c < nc; ++c) M = fmaxf(M, cl.map_shared_rank(pair, c)->x);
+  L = 0.f;
+  if (M != kNegInf)
+    for (unsigned c = 0; c < nc; ++c) {
+      const float2 q = *cl.map_shared_rank(pair, c);
+      if (q.x != kNegInf) L += q.y * ex2_approx((q.x - M) * kLog2e);
+    }
+  cl.sync();  // no CTA leaves while a peer may still read its pair
+}
+
+// Shared-memory-resident slice. The slice [seg0, seg0 + n) of row
+// blockIdx / nc is staged in dynamic shared memory as T; float input keeps
+// the probabilities in place, bf16 input keeps x and recomputes the exp.
+template <typename T, bool kCluster>
+__global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y, int64_t cols,
+                                                                int64_t seg_len, int bulk,
+                                                                int* status) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  T* xs = reinterpret_cast<T*>(smem_raw);
+  __shared__ float red[32];
+  __shared__ float2 pair;
+  __shared__ uint64_t bars[kMaxPieces];
+  __shared__ int abort_flag;
+  const int nc = kCluster ? static_cast<int>(cg::this_cluster().num_blocks()) : 1;
+  const int64_t row = blockIdx.x / nc;
+  const int64_t c = blockIdx.x % nc;
+  const int64_t seg0 = c * seg_len;
+  const int64_t n = min64(cols, seg0 + seg_len) - seg0;  // may be <= 0 for a last CTA
+  const T* xr = x + row * cols + seg0;
+  T* yr = y + row * cols + seg0;
+  constexpr int kPerPiece = kPiece / sizeof(T);
+  const int npieces = n > 0 ? static_cast<int>((n + kPerPiece - 1) / kPerPiece) : 0;
+
+  // ---- stage the slice
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (bulk) {
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < npieces; ++i) mbar_init(&bars[i], 1);
+      fence_barrier_init();
+      const uint64_t pol = policy_evict_first();
+      for (int i = 0; i < npieces; ++i) {
+        const int64_t e0 = int64_t(i) * kPerPiece;
+        const uint32_t bytes = static_cast<uint32_t>(min64(kPerPiece, n - e0) * sizeof(T));
+        mbar_arrive_expect_tx(&bars[i], bytes);
+        bulk_load(xs + e0, xr + e0, bytes, &bars[i], pol);
+      }
+    }
+  } else {
+    for (int64_t e = threadIdx.x; e < n; e += kThreads) xs[e] = xr[e];
+  }
+  __syncthreads();
+  // ---- reduction 1: maximum (piece by piece as the copies land)
+  float m = kNegInf;
+  bool ok = true;
+  for (int i = 0; i < npieces; ++i) {
+    if (bulk && !(ok = mbar_wait_warp(&bars[i], 0, status, dev_code(kDevTimeout, kKerSoftmax, 1),
+                                      &abort_flag)))
+      break;
+    const int64_t e1 = min64(n, int64_t(i + 1) * kPerPiece);
+    for (int64_t e = int64_t(i) * kPerPiece + threadIdx.x; e < e1; e += kThreads)
+      m = fmaxf(m, to_f(xs[e]));
+  }
+  m = block_max(m, red);
+  const float ms = (m == kNegInf) ? 0.f : m;
+  // ---- reduction 2: sum of exp(x - m); float input keeps p in place
+  float l = 0.f;
+  if (ok) {
+    if constexpr (sizeof(T) == 4) {
+      for (int64_t e = threadIdx.x; e < n; e += kThreads) {
+        const float p = exp_shift(xs[e], ms);
+        xs[e] = p;
+        l += p;
+      }
+    } else {
+      for (int64_t e = threadIdx.x; e < n; e += kThreads) l += exp_shift(to_f(xs[e]), ms);
+    }
+  }
+  l = block_sum(l, red);
+  float scale;
+  if constexpr (kCluster) {
+    float M, L;
+    cluster_combine(m, l, &pair, M, L);
+    scale = (L > 0.f && m != kNegInf) ? ex2_approx((m - M) * kLog2e) / L : 0.f;
+  } else {
+    scale = l > 0.f ? 1.f / l : 0.f;
+  }
+  if (abort_flag) {  // uniform: set before the last block reduction
+    // never leave with copies in flight
+    if (bulk && threadIdx.x == 0)
+      for (int i = 0; i < npieces; ++i)
+        mbar_wait(&bars[i], 0, status, dev_code(kDevTimeout, kKerSoftmax, 2), nullptr);
+    return;
+  }
+  // ---- y = p * scale, 16-byte stores where the slice allows
+  if constexpr (sizeof(T) == 4) {
+    if (bulk) {
+      const float4* ps = reinterpret_cast<const float4*>(xs);
+      float4* yv = reinterpret_cast<float4*>(yr);
+      for (int64_t e = threadIdx.x; e < n / 4; e += kThreads) {
+        float4 v = ps[e];
+        v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
+        yv[e] = v;
+      }
+      for (int64_t e = (n / 4) * 4 + threadIdx.x; e < n; e += kThreads) yr[e] = xs[e] * scale;
+    } else {
+      for (int64_t e = threadIdx.x; e < n; e += kThreads) yr[e] = xs[e] * scale;
+    }
+  } else {
+    if (bulk) {
+      const uint4* xv = reinterpret_cast<const uint4*>(xs);
+      uint4* yv = reinterpret_cast<uint4*>(yr);
+      for (int64_t e = threadIdx.x; e < n / 8; e += kThreads) {
+        const uint4 w = xv[e];
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = exp_shift(__uint_as_float(in[j] << 16), ms) * scale;
+          const float hi = exp_shift(__uint_as_float(in[j] & 0xffff0000u), ms) * scale;
+          out[j] = pack_bf16x2(lo, hi);
+        }
+        yv[e] = make_uint4(out[0], out[1], out[2], out[3]);
+      }
+      for (int64_t e = (n / 8) * 8 + threadIdx.x; e < n; e += kThreads)
+        yr[e] = __float2bfloat16_rn(exp_shift(to_f(xs[e]), ms) * scale);
+    } else {
+      for (int64_t e = threadIdx.x; e < n; e += kThreads)
+        yr[e] = __float2bfloat16_rn(exp_shift(to_f(xs[e]), ms) * scale);
+    }
+  }
+}
+
+// Streaming mode: rows longer than a cluster holds on chip.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y, int64_t cols,
+                                                                int64_t seg_len) {
+  __shared__ float red[32];
+  __shared__ float2 pair;
+  const int nc = static_cast<int>(cg::this_cluster().num_blocks());
+  const int64_t row = blockIdx.x / nc;
+  const int64_t c = blockIdx.x % nc;
+  const int64_t seg0 = c * seg_len;
+  const int64_t seg1 = min64(cols, seg0 + seg_len);
+  const T* xr = x + row * cols;
+  T* yr = y + row * cols;
+  // pass 1: per-thread running (m, l), rescaled whenever m grows
+  float m = kNegInf, l = 0.f;
+  for (int64_t e = seg0 + threadIdx.x; e < seg1; e += kThreads) {
+    const float v = to_f(xr[e]);
+    if (v > m) {
+      l = (m == kNegInf) ? 0.f : l * ex2_approx((m - v) * kLog2e);
+      m = v;
+    }
+    if (m != kNegInf) l += exp_shift(v, m);
+  }
+  // merge the threads' states: block max, then rescaled block sum
+  const float bm = block_max(m, red);
+  float lt = (m == kNegInf) ? 0.f : l * ex2_approx((m - bm) * kLog2e);
+  lt = block_sum(lt, red);
+  float M, L;
+  cluster_combine(bm, lt, &pair, M, L);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float Ms = (M == kNegInf) ? 0.f : M;
+  // pass 2: write y
+  for (int64_t e = seg0 + threadIdx.x; e < seg1; e += kThreads)
+    yr[e] = static_cast<T>(exp_shift(to_f(xr[e]), Ms) * inv);
+}
+
+template <typename T>
+cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStream_t s,
+                         int* status) {
+  constexpr int64_t cap = kSliceBytes / sizeof(T);  // elements per CTA on chip
+  constexpr int64_t vec = 16 / sizeof(T);
+  // bulk copies need 16-byte aligned slices of whole 16-byte vectors
+  const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(y) % 16 == 0) && cols % vec == 0;
+  if (cols <= cap) {
+    const size_t smem = size_t((cols * sizeof(T) + 15) / 16 * 16);
+    cudaError_t e = cudaFuncSetAttribute(softmax_rows_onchip<T, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSliceBytes);
+    if (e != cudaSuccess) return e;
+    softmax_rows_onchip<T, false><<<static_cast<unsigned>(rows), kThreads, smem, s>>>(
+        x, y, cols, cols, aligned ? 1 : 0, status);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.stream = s;
+  cfg.blockDim = dim3(kThreads);
+  if (cols <= cap * kMaxCluster) {
+    const int nc = static_cast<int>((cols + cap - 1) / cap);
+    // equal slices, each a whole number of 16-byte vectors
+    int64_t seg = (cols + nc - 1) / nc;
+    seg = (seg + vec - 1) / vec * vec;
+    const size_t smem = size_t(seg * sizeof(T));
+    cudaError_t e = cudaFuncSetAttribute(softmax_rows_onchip<T, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSliceBytes);
+    if (e != cudaSuccess) return e;
+    attr[0].val.clusterDim.x = nc;
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * nc));
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, softmax_rows_onchip<T, true>, x, y, cols, seg,
+                              aligned ? 1 : 0, status);
+  }
+  const int nc = kMaxCluster;
+  const int64_t seg = (cols + nc - 1) / nc;
+  attr[0].val.clusterDim.x = nc;
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * nc));
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, softmax_rows_stream<T>, x, y, cols, seg);
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols, rf_dtype dt,
+                                cudaStream_t s, int* status) {
+  if (rows * kMaxCluster > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (dt == RF_F32)
+    return launch_typed<float>(static_cast<const float*>(x), static_cast<float*>(y), rows, cols,
+                               s, status);
+  return launch_typed<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x),
+                                     static_cast<__nv_bfloat16*>(y), rows, cols, s, status);
+}
+
+}  // namespace rf

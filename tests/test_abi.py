@@ -1,0 +1,147 @@
+"""The C ABI without a GPU: the library loads, exports every function
+include/rf.h declares, and rejects invalid arguments on the host (no CUDA
+call is made before validation, so these run on a machine without a GPU)."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from online_softmax_attention_rf_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rf.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return api.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rf_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for required in ("rf_softmax_rows", "rf_attn_fwd", "rf_attn_decode_splitk",
+                     "rf_splitk_merge"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = _declared()
+    assert names
+    for n in names:
+        assert hasattr(L, n), n
+    # the binding mirrors the header one to one
+    assert sorted(api.SIGNATURES) == names
+
+
+def test_version_and_workspace_size(L):
+    assert L.rf_version() == 1
+    n = 16 * 32 * 32 * 129 * 4
+    assert api.decode_workspace_bytes(16, 32, 32, 128) == (n + 255) // 256 * 256
+    assert api.decode_workspace_bytes(0, 32, 32, 128) == 0
+
+
+A = 0x10000        # a 16-byte-aligned fake device address; never dereferenced
+MIS = 0x10008      # misaligned for TMA
+
+
+def _attn(L, q=A, k=A, v=A, o=A, lse=A, B=1, H=4, Hkv=2, Sq=256, Sk=256, d=128, scale=0.1,
+          causal=0, bm=None, dt=api.RF_BF16):
+    return L.rf_attn_fwd(q, k, v, o, lse, B, H, Hkv, Sq, Sk, d, scale, causal, bm, dt, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Hkv=3), api.RF_ERR_INVALID),               # H % Hkv
+    (dict(scale=0.0), api.RF_ERR_INVALID),
+    (dict(scale=-1.0), api.RF_ERR_INVALID),
+    (dict(scale=math.nan), api.RF_ERR_INVALID),
+    (dict(scale=math.inf), api.RF_ERR_INVALID),
+    (dict(causal=2), api.RF_ERR_INVALID),
+    (dict(B=0), api.RF_ERR_INVALID),
+    (dict(Sq=-1), api.RF_ERR_INVALID),
+    (dict(d=96), api.RF_ERR_UNSUPPORTED),            # bf16 head dims: 64, 128
+    (dict(d=258, dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
+    (dict(d=66, dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
+    (dict(dt=7), api.RF_ERR_INVALID),
+    (dict(q=None), api.RF_ERR_INVALID),
+    (dict(k=None), api.RF_ERR_INVALID),
+    (dict(o=None), api.RF_ERR_INVALID),
+    (dict(q=MIS), api.RF_ERR_INVALID),
+    (dict(v=MIS), api.RF_ERR_INVALID),
+    (dict(lse=A + 2), api.RF_ERR_INVALID),
+])
+def test_attn_fwd_rejects(L, kw, expect):
+    assert _attn(L, **kw) == expect
+    assert L.rf_last_error()
+
+
+def test_attn_fwd_empty_query_is_a_no_op(L):
+    assert _attn(L, q=None, o=None, Sq=0) == api.RF_OK
+
+
+@pytest.mark.parametrize("field,value", [
+    ("tile_q", 64), ("tile_k", 256), ("nqt", 3), ("nkt", 1), ("per_head", 2), ("row_ptr", 0),
+    ("col_idx", 0)])
+def test_attn_fwd_rejects_bad_blockmask(L, field, value):
+    bm = api.RFBlockMask(128, 128, 2, 2, A, A, 0)
+    setattr(bm, field, value)
+    assert _attn(L, bm=ctypes.byref(bm)) == api.RF_ERR_INVALID
+
+
+def _decode(L, q=A, k=A, v=A, o=A, lse=A, B=2, H=8, Hkv=2, Sk=1000, d=128, scale=0.1, nsplit=4,
+            ws=A, ws_bytes=None, dt=api.RF_BF16):
+    if ws_bytes is None:
+        ws_bytes = api.decode_workspace_bytes(B, H, nsplit, d)
+    return L.rf_attn_decode_splitk(q, k, v, o, lse, B, H, Hkv, Sk, d, scale, nsplit, ws, ws_bytes,
+                                   dt, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(nsplit=0), api.RF_ERR_INVALID),
+    (dict(nsplit=1001), api.RF_ERR_INVALID),        # more splits than keys
+    (dict(ws_bytes=16), api.RF_ERR_INVALID),
+    (dict(ws=None), api.RF_ERR_INVALID),
+    (dict(ws=MIS), api.RF_ERR_INVALID),
+    (dict(Hkv=3), api.RF_ERR_INVALID),
+    (dict(H=64, Hkv=2), api.RF_ERR_UNSUPPORTED),    # 32 query heads per kv head
+    (dict(dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
+    (dict(d=96), api.RF_ERR_UNSUPPORTED),
+    (dict(scale=0.0), api.RF_ERR_INVALID),
+    (dict(Sk=0), api.RF_ERR_INVALID),
+])
+def test_decode_rejects(L, kw, expect):
+    assert _decode(L, **kw) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A, A, A, A, 5, 0, 64, api.RF_BF16), api.RF_ERR_INVALID),      # nsplit 0
+    ((A, A, A, A, 5, 4, 2048, api.RF_BF16), api.RF_ERR_INVALID),    # d > 1024
+    ((A, A, A, A, -1, 4, 64, api.RF_BF16), api.RF_ERR_INVALID),
+    ((None, A, A, A, 5, 4, 64, api.RF_BF16), api.RF_ERR_INVALID),
+    ((A, A, A, A, 0, 4, 64, api.RF_BF16), api.RF_OK),               # no rows: no launch
+])
+def test_merge_validation(L, args, expect):
+    o_part, lse_part, o, lse, rows, nsplit, d, dt = args
+    assert L.rf_splitk_merge(o_part, lse_part, o, lse, rows, nsplit, d, dt, None) == expect
+
+
+def test_softmax_and_blockmask_validation(L):
+    assert L.rf_softmax_rows(A, A, -1, 5, api.RF_F32, None) == api.RF_ERR_INVALID
+    assert L.rf_softmax_rows(A, A, 5, 5, 9, None) == api.RF_ERR_INVALID
+    assert L.rf_softmax_rows(None, A, 5, 5, api.RF_F32, None) == api.RF_ERR_INVALID
+    assert L.rf_softmax_rows(A, A, 0, 5, api.RF_F32, None) == api.RF_OK
+    assert L.rf_blockmask_build(A, 1, 4, 0, A, A, 16, None) == api.RF_ERR_INVALID
+    assert L.rf_blockmask_build(None, 1, 4, 4, A, A, 16, None) == api.RF_ERR_INVALID
+    assert L.rf_blockmask_build(A, 1, 4, 4, A, A, -1, None) == api.RF_ERR_INVALID
+    assert L.rf_debug_set_visited(A, 0) == api.RF_ERR_INVALID
+    assert L.rf_debug_set_visited(None, 0) == api.RF_OK
+    assert L.rf_device_status(None, None) == api.RF_ERR_INVALID

@@ -1,0 +1,144 @@
+"""Split-K decode, the log-sum-exp merge, row softmax and the block-list build
+on the GPU against the float64 oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_softmax_attention_rf_gb300 import api, inputs
+from tests.helpers import (TOL_BF16_LSE, TOL_BF16_O, TOL_BF16_SOFTMAX, TOL_F32, assert_close,
+                           f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,H,Hkv,Sk,d,nsplit", [
+    (2, 8, 2, 5000, 128, 7),       # G = 4, ragged last split
+    (1, 4, 4, 3000, 128, 3),       # G = 1 (padded to 4)
+    (2, 16, 2, 4096, 64, 16),      # G = 8, d = 64
+    (1, 16, 1, 999, 128, 5),       # G = 16
+    (1, 2, 1, 100, 64, 100),       # one key per split
+    (3, 6, 2, 130, 128, 1),        # G = 3, a single split
+])
+def test_decode_matches_oracle(cuda_device, B, H, Hkv, Sk, d, nsplit):
+    q, k, v = inputs.make_qkv(B, H, Hkv, 1, Sk, d, 31, "bf16")
+    scale = inputs.default_scale(d)
+    ws_bytes = api.decode_workspace_bytes(B, H, nsplit, d)
+    ws = torch.empty(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    o, lse = api.attn_decode_splitk(q.cuda(), k.cuda(), v.cuda(), nsplit, scale, ws)
+    assert api.device_status() == 0
+    # the merged result equals the unsplit definition ...
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), scale)
+    assert_close(o, o_ref, TOL_BF16_O, "O")
+    assert_close(lse, lse_ref, TOL_BF16_LSE, "LSE")
+    # ... and the stored partials equal the per-split definition
+    n = B * H * nsplit
+    op_ref, lp_ref = oracle.decode_partials(f64(q), f64(k), f64(v), scale, nsplit)
+    assert_close(ws[:n * d].view(B, H, nsplit, d), op_ref, 5e-3, "O_s")
+    assert_close(ws[n * d:n * d + n].view(B, H, nsplit), lp_ref, TOL_BF16_LSE, "lse_s")
+
+
+def test_decode_split_count_does_not_change_the_result(cuda_device):
+    q, k, v = (t.cuda() for t in inputs.make_qkv(2, 8, 2, 1, 8192, 128, 32, "bf16"))
+    o1, l1 = api.attn_decode_splitk(q, k, v, 1)
+    for ns in (2, 8, 32, 128):
+        o, l = api.attn_decode_splitk(q, k, v, ns)
+        assert_close(o, f64(o1), TOL_BF16_O, "O nsplit=%d" % ns)
+        assert_close(l, f64(l1), TOL_BF16_LSE, "LSE nsplit=%d" % ns)
+
+
+def test_decode_equals_prefill_row(cuda_device):
+    # FlashDecoding and FlashAttention are special cases of one form: the
+    # decode of one query row equals the prefill kernel on that row
+    q, k, v = (t.cuda() for t in inputs.make_qkv(2, 8, 2, 1, 3000, 128, 33, "bf16"))
+    od, ld = api.attn_decode_splitk(q, k, v, 6)
+    op, lp = api.attn_fwd(q, k, v)
+    assert_close(od, f64(op), TOL_BF16_O, "O")
+    assert_close(ld, f64(lp), TOL_BF16_LSE, "LSE")
+
+
+def _partials(rows, nsplit, d, seed):
+    rng = np.random.default_rng(seed)
+    o_part = rng.standard_normal((rows, nsplit, d)).astype(np.float32)
+    lse_part = (rng.standard_normal((rows, nsplit)) * 3).astype(np.float32)
+    lse_part[1, 3] = -np.inf                   # an empty split
+    lse_part[2, :] = -np.inf                   # a row with nothing at all
+    lse_part[3, :] += 80.0                     # large values must not overflow
+    return o_part, lse_part
+
+
+@pytest.mark.parametrize("rows,nsplit,d", [(5, 4, 64), (37, 32, 128), (9, 7, 100), (4, 130, 33)])
+def test_merge_matches_oracle(cuda_device, rows, nsplit, d):
+    o_part, lse_part = _partials(rows, nsplit, d, rows)
+    o, lse = api.splitk_merge(torch.from_numpy(o_part).cuda(), torch.from_numpy(lse_part).cuda(),
+                              torch.float32)
+    o_ref, lse_ref = oracle.merge_partials(o_part, lse_part)
+    assert_close(o, o_ref, TOL_F32, "O")
+    assert_close(lse, lse_ref, TOL_F32 * 100, "LSE")   # |LSE| ~ 90: 1e-5 relative
+    ob, _ = api.splitk_merge(torch.from_numpy(o_part).cuda(), torch.from_numpy(lse_part).cuda(),
+                             torch.bfloat16)
+    assert_close(ob, o_ref, 8e-3 * max(1.0, float(np.abs(o_ref).max())), "O bf16")
+
+
+SOFTMAX_SHAPES = [
+    (7, 33), (64, 1000), (3, 1), (16, 16384), (2, 32768), (3, 40000), (2, 262144),
+    (1, 300001), (2, 600000), (5, 4099)]
+
+
+@pytest.mark.parametrize("rows,cols", SOFTMAX_SHAPES)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_softmax_rows_matches_oracle(cuda_device, rows, cols, dtype):
+    x = inputs.make_rows(rows, cols, rows * 7 + cols, dtype, 3.0)
+    y = api.softmax_rows(x.cuda())
+    assert api.device_status() == 0
+    y_ref = oracle.softmax_rows(f64(x))
+    assert_close(y, y_ref, TOL_F32 if dtype == "f32" else TOL_BF16_SOFTMAX, "y")
+
+
+def test_softmax_rows_edge_values(cuda_device):
+    x = torch.randn(4, 5000) * 2
+    x[0, 100:] = -math.inf            # masked tail
+    x[1, :] = -math.inf               # nothing visible: zeros
+    x[2, 7] = 1e4                     # one dominant entry
+    y = api.softmax_rows(x.cuda())
+    y_ref = oracle.softmax_rows(f64(x))
+    assert_close(y, y_ref, TOL_F32, "y")
+    # in place
+    xc = x.cuda()
+    api.softmax_rows(xc, out=xc)
+    assert_close(xc, y_ref, TOL_F32, "y in place")
+
+
+def test_blockmask_build_matches_enumeration(cuda_device):
+    tm = inputs.random_tile_mask(50, 77, 0.3, 9, nheads=3)
+    tm[1, 4, :] = False
+    tm[2, 0, :] = True
+    bm = api.BlockMask.from_dense(tm)
+    assert api.device_status() == 0
+    row_ptr, col_idx = oracle.bsr_from_tile_mask(tm)
+    got_rp = bm.row_ptr.cpu().numpy()
+    assert np.array_equal(got_rp, row_ptr)
+    assert np.array_equal(bm.col_idx.cpu().numpy()[:row_ptr[-1]], col_idx)
+
+
+def test_blockmask_build_block_sparse_workload(cuda_device):
+    w = inputs.WORKLOADS["block_sparse"]
+    tm = inputs.window_random_tile_mask(inputs.n_tiles(w["Sq"]), w["window"], w["frac"], w["seed"])
+    bm = api.BlockMask.from_dense(tm)
+    row_ptr, col_idx = oracle.bsr_from_tile_mask(tm)
+    assert int(bm.row_ptr[-1]) == 1722 == row_ptr[-1]
+    assert np.array_equal(bm.col_idx.cpu().numpy()[:1722], col_idx)
+
+
+def test_blockmask_build_capacity_is_reported(cuda_device):
+    dense = torch.ones(1, 4, 4, dtype=torch.uint8, device="cuda")
+    row_ptr = torch.empty(5, dtype=torch.int32, device="cuda")
+    col_idx = torch.full((10,), -1, dtype=torch.int32, device="cuda")
+    api.blockmask_build(dense, row_ptr, col_idx)
+    with pytest.raises(api.RFError):
+        api.device_status()
+    assert row_ptr.tolist() == [0, 4, 8, 12, 16]
+    assert col_idx.tolist() == [0, 1, 2, 3, 0, 1, 2, 3, 0, 1]
