@@ -1,0 +1,447 @@
+"""Benchmark of the fused online-softmax attention path on GB300.
+
+One step = one attention forward (rf_attn_fwd) over the causal multi-head
+prefill workload: B=4, H=32, Sq=Sk=4096, d=128, bf16 in / fp32 accumulate,
+inputs seeded-synthetic and resident in HBM. The JSON line reports
+  value      algorithmic TFLOP/s (4*d flops per visible query-key pair),
+  e2e        the same metric through the public API with host buffers
+             (pinned host -> device copies of Q, K, V and device -> host
+             copies of O and LSE inside the timed region),
+  roofline   the attention kernel against the measured dense bf16 peak,
+  decode     the split-K decode workload (B=16, Hq=32, Hkv=8, Sk=65536,
+             32 splits) in GB/s against the measured HBM copy bandwidth,
+  softmax    row softmax over a [16384 x 16384] fp32 matrix in GB/s,
+  cpu_baseline  the float64 oracle on the host cores on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torch.distributed.run; each rank runs the full workload on
+its own GPU (weak scaling, no collective on the data path) and the slowest
+rank's time is reported for the aggregate.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from online_softmax_attention_rf_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "mha_prefill"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch from ncu captures (profiles/), valid only for the
+# kernel source they were taken on; any change to the source makes it null.
+TRAFFIC = {
+    # profiles/attn_tc_mha_prefill.md: dram read 1.996 GB + write 0.125 GB
+    "attn_tc_mha_prefill": {"digest": "9b5c5b0161a2f2a8", "bytes": 2121915904},
+}
+
+
+def source_digest(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "online_softmax_attention_rf_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def visible_pairs(w, tile_mask=None):
+    """Unmasked (query, key) pairs per head (the algorithmic work)."""
+    Sq, Sk = w["Sq"], w["Sk"]
+    if tile_mask is not None:
+        rows = np.arange(Sq)
+        total = 0
+        T = w.get("tile", 128)
+        for qt in range(tile_mask.shape[0]):
+            r = rows[qt * T:(qt + 1) * T]
+            for kt in np.nonzero(tile_mask[qt])[0]:
+                keys = min(Sk, (kt + 1) * T) - kt * T
+                if w["causal"]:
+                    lim = np.minimum(Sk, r + 1 + Sk - Sq) - kt * T
+                    total += int(np.clip(lim, 0, keys).sum())
+                else:
+                    total += len(r) * keys
+        return total
+    if w["causal"]:
+        i = np.arange(Sq, dtype=np.int64)
+        return int(np.clip(i + 1 + Sk - Sq, 0, Sk).sum())
+    return Sq * Sk
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def max_over_ranks(dist, x):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+_INPUT_CACHE = {}
+
+
+def cpu_oracle_sample(name, budget_s=12.0):
+    """Time the float64 oracle on whole heads of the workload until the budget
+    is spent; returns (TFLOP/s, seconds, heads, cores)."""
+    import oracle
+    w = inputs.WORKLOADS[name]
+    if name not in _INPUT_CACHE:
+        _INPUT_CACHE[name] = inputs.workload_inputs(name)
+    q, k, v, scale, extras = _INPUT_CACHE[name]
+    tm = extras.get("tile_mask")
+    G = w["H"] // w["Hkv"]
+    pairs = visible_pairs(w, tm)
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    heads = 0
+    for b in range(w["B"]):
+        for h in range(w["H"]):
+            oracle.attention(q[b:b + 1, h:h + 1].double().numpy(),
+                             k[b:b + 1, h // G:h // G + 1].double().numpy(),
+                             v[b:b + 1, h // G:h // G + 1].double().numpy(), scale, w["causal"], tm)
+            heads += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w["d"] * pairs * heads
+    return flops / dt / 1e12, dt, heads, cores
+
+
+def run_reference(args, dist, rank):
+    """The oracle as the reference arm, on the host cores."""
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[WORKLOAD]
+    vals = []
+    for _ in range(args.warmup):
+        cpu_oracle_sample(WORKLOAD, budget_s=2.0)
+    t0 = time.perf_counter()
+    samples = []
+    per_step = min(8.0, 150.0 / args.steps)
+    for _ in range(args.steps):
+        v, dt, heads, cores = cpu_oracle_sample(WORKLOAD, budget_s=per_step)
+        vals.append(v)
+        samples.append(heads)
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": "attn fwd TFLOP/s (prefill)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * elapsed / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, **{kk: w[kk] for kk in ("B", "H", "Hkv", "Sq", "Sk", "d",
+                                                               "causal")}},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "whole heads of the workload per step (%s heads), float64 "
+                                   "three-pass NumPy oracle" % samples},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_steps(fn, steps, warmup, stream, dist):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, per_launch
+
+
+def run_ours(args, dist, rank, world, local):
+    from online_softmax_attention_rf_gb300 import api
+    api.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    if args.only in ("decode", "softmax"):
+        # one workload alone (used for profiling captures)
+        fn = bench_decode if args.only == "decode" else bench_softmax
+        out = fn(args, dev, stream, peaks, peak_src)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
+    w = inputs.WORKLOADS[WORKLOAD]
+    q_h, k_h, v_h, scale, _ = inputs.workload_inputs(WORKLOAD)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    flops = 4.0 * w["d"] * visible_pairs(w) * w["B"] * w["H"]
+
+    def step():
+        api.attn_fwd(q, k, v, scale, w["causal"], None, o, lse)
+
+    with ClockSampler(local) as clk:
+        total_ms, per_launch = time_steps(step, args.steps, args.warmup, stream, dist)
+    total_ms = max_over_ranks(dist, total_ms)
+    ms_step = total_ms / args.steps
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    assert api.device_status() == 0
+
+    att_ms = statistics.mean(per_launch)
+    achieved = flops / (att_ms * 1e-3) / 1e12
+    tc_digest = source_digest("attn_tc.cu", "rf_device.cuh")
+    traffic = TRAFFIC.get("attn_tc_mha_prefill")
+    traffic = traffic["bytes"] if traffic and traffic["digest"] == tc_digest else None
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": "%s dense bf16 (burst)" % peak_src,
+                "frac_sustained": achieved / peaks.get("bf16_tflops_sustained",
+                                                       peaks["bf16_tflops"])}
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    if args.only == "prefill":
+        if rank == 0:
+            print(json.dumps({"workload": WORKLOAD, "value": value, "unit": "TFLOP/s",
+                              "ms_per_step": ms_step, "roofline": roofline}), flush=True)
+        return
+
+    # end to end through the public API with host buffers (fresh device tensors)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        api.attn_fwd(q, k, v, scale, w["causal"], None, o, lse)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    n_e2e = max(3, min(args.steps, 50))
+    e2e_total, _ = time_steps(e2e_step, n_e2e, 3, stream, dist)
+    e2e_total = max_over_ranks(dist, e2e_total)
+    e2e_ms = e2e_total / n_e2e
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    del q, k, v, o, lse, qp, kp, vp, op, lp
+    torch.cuda.empty_cache()
+
+    decode = bench_decode(args, dev, stream, peaks, peak_src)
+    softmax = bench_softmax(args, dev, stream, peaks, peak_src)
+    launches = args.steps
+
+    if rank != 0:
+        return
+    cpu_v, cpu_dt, cpu_heads, cores = cpu_oracle_sample(WORKLOAD)
+    line = {
+        "metric": "attn fwd TFLOP/s (prefill); decode GB/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": w["B"], "H": w["H"], "Hkv": w["Hkv"],
+                   "Sq": w["Sq"], "Sk": w["Sk"], "d": w["d"], "causal": w["causal"],
+                   "parallelism": "dp%d (independent replicas)" % world,
+                   "l2": "inputs larger than L2 (Q, K, V, O = 537 MB per step)"},
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "clocks": clk.summary(),
+        "decode": decode,
+        "softmax": softmax,
+        "cpu_baseline": {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d whole heads of the workload (%.1f s, float64 three-pass "
+                                   "NumPy oracle)" % (cpu_heads, cpu_dt)},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def side_steps(args):
+    """Timed steps for the secondary workloads (decode, row softmax)."""
+    return max(5, min(args.steps, 50))
+
+
+def bench_decode(args, dev, stream, peaks, peak_src):
+    from online_softmax_attention_rf_gb300 import api
+    w = inputs.WORKLOADS["decode_splitk"]
+    q_h, k_h, v_h, scale, _ = inputs.workload_inputs("decode_splitk")
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    ws = torch.empty(api.decode_workspace_bytes(w["B"], w["H"], w["nsplit"], w["d"]) // 4,
+                     dtype=torch.float32, device=dev)
+    algo = (k.numel() + v.numel() + q.numel() + o.numel()) * 2 + lse.numel() * 4
+
+    def step():
+        api.attn_decode_splitk(q, k, v, w["nsplit"], scale, ws, o, lse)
+
+    # K and V (4.3 GB) are far larger than L2: no flush needed
+    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    ms = statistics.mean(per)
+    gbs = algo / (ms * 1e-3) / 1e9
+    assert api.device_status() == 0
+    out = {"workload": "decode_splitk", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+           "algorithmic_bytes": algo,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "frac_of_8TBs": gbs / 8000.0,
+                        "traffic": None, "peak_source": "%s HBM copy" % peak_src,
+                        "note": "step = partials kernel + merge kernel"}}
+    del q, k, v, o, lse, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_softmax(args, dev, stream, peaks, peak_src):
+    from online_softmax_attention_rf_gb300 import api
+    sw = inputs.SOFTMAX_WORKLOADS["rows_64k"]
+    x = inputs.make_rows(sw["rows"], sw["cols"], sw["seed"]).to(dev)
+    y = torch.empty_like(x)
+    algo = 2 * x.numel() * 4
+
+    def step():
+        api.softmax_rows(x, y)
+
+    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    ms = statistics.mean(per)
+    gbs = algo / (ms * 1e-3) / 1e9
+    out = {"workload": "rows_64k [16384 x 16384] f32", "value": gbs, "unit": "GB/s",
+           "ms_per_step": ms,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "frac_of_8TBs": gbs / 8000.0,
+                        "traffic": None, "peak_source": "%s HBM copy" % peak_src}}
+    del x, y
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax"], default="all",
+                    help="time one workload alone (for profiling); the default runs all")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist, rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist, rank)
+        else:
+            run_ours(args, dist, rank, world, local)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ready and its P being consumed, and K/V slots are released as early as
     // their last reader is issued (commit-tracked).
     if (lane == 0) {
-      UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, false)};
+      UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, true)};
       const uint32_t q_s[2] = {s_base + L::kOffQ, s_base + L::kOffQ + L::kTileBytes};
       const uint32_t p_s[2] = {s_base + L::kOffP, s_base + L::kOffP + kBM * kBN * 2};
       const uint32_t tm_s[2] = {tmem + L::kTmemS, tmem + L::kTmemS + kBN};
