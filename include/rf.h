@@ -148,6 +148,31 @@ rf_status rf_attn_decode_splitk(const void *q, const void *k, const void *v, voi
                                 float scale, int nsplit, float *ws, size_t ws_bytes,
                                 rf_dtype dt, rf_stream stream);
 
+/*
+ * Split-K decode without a caller workspace (no counterpart on the pages:
+ * an addition for callers that cannot allocate device memory, e.g. a plug-in
+ * inside a host process whose runtime owns all device memory, or a serving
+ * loop that forbids allocation after start-up).
+ * Same arguments, results and errors as rf_attn_decode_splitk, minus ws and
+ * ws_bytes: the partials live in a 16 MiB array inside the library's device
+ * image, reserved on every GPU that loads the library until the process
+ * exits. Allocates nothing (no cudaMalloc/cudaFree, no allocating library
+ * call).
+ *  - Sizes whose workspace, rf_decode_workspace_bytes(B,H,nsplit,d), exceeds
+ *    16 MiB (16777216 bytes) are rejected with RF_ERR_INVALID.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's partials; each call writes every partial before reading it, so
+ *    nothing needs clearing, but calls that overlap on the GPU (different
+ *    streams, or concurrent host threads) race on it and must be serialised
+ *    by the caller.
+ */
+rf_status rf_attn_decode_splitk_noalloc(const void *q, const void *k, const void *v, void *o,
+                                        float *lse, int B, int H, int Hkv, int Sk, int d,
+                                        float scale, int nsplit, rf_dtype dt, rf_stream stream);
+
 /* Bytes of workspace rf_attn_decode_splitk needs: 4 * B*H*nsplit*(d + 1),
  * rounded up to 256. Returns 0 for non-positive arguments. */
 size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d);

@@ -50,6 +50,8 @@ SIGNATURES = {
                          ctypes.POINTER(RFBlockMask), _I, _P]),
     "rf_attn_decode_splitk": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I,
                                    _P]),
+    "rf_attn_decode_splitk_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I,
+                                           _P]),
     "rf_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "rf_splitk_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P]),
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
@@ -203,6 +205,25 @@ def attn_decode_splitk(q, k, v, nsplit, scale=None, workspace=None, out=None, ls
                                        Sk, d, float(scale), nsplit, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _dt(q),
                                        _stream()))
+    return o, lse
+
+
+def attn_decode_splitk_noalloc(q, k, v, nsplit, scale=None, out=None, lse=None):
+    """rf_attn_decode_splitk_noalloc: the split-K decode with the library's own
+    fixed 16 MiB device workspace (for callers that cannot allocate; calls on
+    one device share that workspace and must not overlap on the GPU)."""
+    _cuda(q, k, v)
+    B, H, Sq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    _cuda(o, lse)
+    _check(lib().rf_attn_decode_splitk_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B,
+                                               H, Hkv, Sk, d, float(scale), nsplit, _dt(q),
+                                               _stream()))
     return o, lse
 
 

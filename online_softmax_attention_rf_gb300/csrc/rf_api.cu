@@ -60,6 +60,8 @@ int* status_word() {
   return static_cast<int*>(p);
 }
 
+rf_status set_last_error(rf_status st, const char* msg) { return fail(st, "%s", msg); }
+
 uint8_t* debug_visited(int64_t* len) {
   if (len != nullptr) *len = g_visited_len;
   return g_visited;

@@ -33,6 +33,9 @@ __host__ __device__ constexpr int dev_code(int kind, int kernel, int site) {
 // Device address of the status word for the current device (nullptr on error).
 int* status_word();
 
+// Sets this thread's rf_last_error() message and returns st.
+rf_status set_last_error(rf_status st, const char* msg);
+
 // Visited-tile debug buffer for the calling host thread (nullptr = off).
 uint8_t* debug_visited(int64_t* len);
 
