@@ -18,19 +18,27 @@
 //   warp 8     TMA producer: Q tiles, then K/V tiles into a shared-memory ring
 //   warp 9     TMEM allocator and MMA issuer (one elected lane)
 // Tensor memory (512 columns): S0 | S1 (128 f32 columns each) | O0 | O1 (D each).
-// Shared memory: Q0, Q1, P0, P1 (bf16, 128-byte swizzled K-major) and the K/V
-// ring (each slot one 128 x D tile; V is read as an MN-major operand).
+// P_t (bf16, two per column) is written back into tensor memory and is the A
+// operand of the P.V MMA, so that MMA reads only V from shared memory: at
+// D = 128 P_t overwrites the first half of S_t, at D = 64 it has its own
+// columns after O1. Shared memory: Q0, Q1 (128-byte swizzled K-major) and the
+// K/V ring (each slot one 128 x D tile; V is read as an MN-major operand).
 //
 // Per key tile u of query tile t:
 //   MMA:     S_t = Q_t K_u^T                      (tcgen05.mma, f32 in TMEM)
 //   softmax: m' = max(m, rowmax S); p = exp2(S*c - m'); l = a*l + rowsum p;
 //            if the max grew by more than 2^8, O_t *= a = exp2(m - m') (in TMEM)
 //            else the stale max is kept (a = 1; exact, since l and O share it);
-//            P_t = bf16(p) into shared memory
+//            P_t = bf16(p) into tensor memory
 //   MMA:     O_t += P_t V_u
 // The MMA lane issues QK0(u), PV1(u'), QK1(u), PV0(u) (u' the previous key
 // tile), so the softmax of each group overlaps about two MMAs of the other.
 // Epilogue: O = O_t / l (bf16), LSE = (m + log2 l) ln 2.
+//
+// Reuse of S_t's columns for P_t relies on the tensor pipe executing one
+// thread's MMAs in issue order: QK_t(u+1) (which overwrites S_t) is issued after
+// PV_t(u) (which reads P_t from it), as in the published Blackwell attention
+// kernels; the softmax only writes P_t(u+1) after PV_t(u) has completed.
 //
 // Every wait is bounded (RF_WAIT_LIMIT_NS); on expiry the kernel records a
 // status code, the other roles notice the abort flag, and the CTA unwinds,
@@ -58,15 +66,19 @@ constexpr int kChunk = 16384;              // one 128-row x 64-column bf16 swizz
 template <int D>
 struct Layout {
   static constexpr int kTileBytes = kBM * D * 2;  // one Q, K or V tile
-  static constexpr int kStages = (D == 128) ? 3 : 6;
+  static constexpr int kStages = (D == 128) ? 5 : 8;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffKV = kOffP + 2 * kBM * kBN * 2;
+  static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemS = 0;        // S0 at 0, S1 at 128
   static constexpr uint32_t kTmemO = 2 * kBN;  // O0 at 256, O1 at 256 + D
+  // P_t: on S_t's first 64 columns at D = 128 (S_t is read into registers
+  // before P_t is written); after O1 at D = 64
+  __host__ __device__ static constexpr uint32_t tmem_p(int t) {
+    return D == 128 ? kTmemS + t * kBN : kTmemO + 2 * D + t * 64;
+  }
 };
 
 struct Bars {
@@ -163,15 +175,16 @@ __device__ __forceinline__ void issue_qk(uint32_t tm_s, uint32_t q_s, uint32_t k
   }
 }
 
+// O_t (+)= P_t V: A = P_t from tensor memory (8 columns per 16 keys),
+// B = V from shared memory as an MN-major operand.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tm_o, uint32_t p_s, uint32_t v_s,
+__device__ __forceinline__ void issue_pv(uint32_t tm_o, uint32_t tm_p, uint32_t v_s,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 1);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    const uint64_t a = sdesc_sw128(p_s + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024);
     const uint64_t b = sdesc_sw128(v_s + kk * 16 * 128, kChunk, 1024);
-    mma_bf16(tm_o, a, b, idesc, (kk > 0 || accumulate) ? 1u : 0u);
+    mma_bf16_ts(tm_o, tm_p + kk * 8, b, idesc, (kk > 0 || accumulate) ? 1u : 0u);
   }
 }
 
@@ -188,10 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_base = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // heavy query-tile pairs first (causal: later tiles see more keys)
-  const int BH = p.B * p.H;
-  const int pair = p.pairs - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // head-major order, so that the CTAs of one head (and of the query heads
+  // that share a kv head) run together and keep its K/V in L2; within a head
+  // the heavy query-tile pairs go first (causal: later tiles see more keys)
+  const int pair = p.pairs - 1 - static_cast<int>(blockIdx.x % p.pairs);
+  const int bh = static_cast<int>(blockIdx.x / p.pairs);
   const int b = bh / p.H, h = bh % p.H;
   const int bk = b * p.Hkv + h / (p.H / p.Hkv);
   const int qt0 = 2 * pair;
@@ -274,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, true)};
       const uint32_t q_s[2] = {s_base + L::kOffQ, s_base + L::kOffQ + L::kTileBytes};
-      const uint32_t p_s[2] = {s_base + L::kOffP, s_base + L::kOffP + kBM * kBN * 2};
+      const uint32_t tm_p[2] = {tmem + L::tmem_p(0), tmem + L::tmem_p(1)};
       const uint32_t tm_s[2] = {tmem + L::kTmemS, tmem + L::kTmemS + kBN};
       const uint32_t tm_o[2] = {tmem + L::kTmemO, tmem + L::kTmemO + D};
       int nq[2] = {0, 0};    // QK tiles issued per query tile
@@ -308,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(&bar.kv_full[vseq % NS], (vseq / NS) & 1, 24)) return false;
         if (!wait(&bar.p_full[t], npv[t] & 1, 25)) return false;
         tc_fence_after_sync();
-        issue_pv<D>(tm_o[t], p_s[t], slot_addr(vseq), npv[t] > 0);
+        issue_pv<D>(tm_o[t], tm_p[t], slot_addr(vseq), npv[t] > 0);
         mma_commit(&bar.o_done[t]);
         ++npv[t];
         return true;
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const TileList list = tile_list(p, bh, qt, false);
     const uint32_t tm_s = tmem + L::kTmemS + t * kBN + lane_off;
     const uint32_t tm_o = tmem + L::kTmemO + t * D + lane_off;
-    unsigned char* p_tile = smem + L::kOffP + t * (kBM * kBN * 2);
+    const uint32_t tm_p = tmem + L::tmem_p(t) + lane_off;
     const int64_t shift = int64_t(p.Sk) - p.Sq;
     const int64_t row_lim = p.causal ? min64(p.Sk, row + 1 + shift) : p.Sk;
     const int64_t tile_first_lim =
@@ -366,72 +380,95 @@ __global__ void __launch_bounds__(kThreads, 1)
                           abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t sr[128];
-      tmem_ld64_wait(tm_s, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
-      tmem_ld64_wait(tm_s + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.s_free[t]);
       // element mask only where the tile crosses the causal diagonal or Sk
       const int64_t k0 = int64_t(u) * kBN;
-      float mx = kNegInf;
-      if (k0 + kBN > tile_first_lim) {
-        const int64_t lim = row_lim - k0;
+      const int lim = (k0 + kBN > tile_first_lim)
+                          ? static_cast<int>(max64(int64_t(0), min64(kBN, row_lim - k0)))
+                          : kBN;
+      // pass 1: row maximum over all 128 columns (one TMEM read), 8
+      // independent partial maxima, two columns per step (max is exact, so
+      // the order does not matter)
+      float mx;
+      {
+        uint32_t sr[128];
+        tmem_ld128_wait(tm_s, sr);
+        if (lim < kBN) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          if (c >= lim) sr[c] = __float_as_uint(kNegInf);
-          mx = fmaxf(mx, __uint_as_float(sr[c]));
+          for (int c = 0; c < kBN; ++c)
+            if (c >= lim) sr[c] = __float_as_uint(kNegInf);
         }
-      } else {
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        for (int i = 0; i < 8; ++i) m8[i] = kNegInf;
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2)
+          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sr[c]),
+                                   __uint_as_float(sr[c + 1]));
+        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
       const float m_new = (mx == kNegInf) ? m_run : fmaxf(m_run, mx * p.scale_log2);
       const bool resc = m_new > m_run + kRescaleThreshold;
       const float m_use = resc ? m_new : m_run;
       const float alpha = resc ? ex2_approx(m_run - m_new) : 1.f;
       const float sh = (m_use == kNegInf) ? 0.f : m_use;
-      float sum = 0.f;
-      uint32_t pw[64];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), p.scale_log2, -sh));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -sh));
-        sum += p0 + p1;
-        pw[c >> 1] = pack_bf16x2(p0, p1);
-      }
-      l_run = l_run * alpha + sum;
-      m_run = m_use;
       if (j > 0) {
-        // the previous P.V must be done: P_t is free and O_t holds its sum
+        // the previous P.V must be done before P_t's columns are rewritten and
+        // O_t is rescaled (it was issued before the QK that produced this S,
+        // so this wait normally returns at once)
         ok = mbar_wait_warp(&bar.o_done[t], (j - 1) & 1, p.status,
                             dev_code(kDevTimeout, kKerAttnTc, 31), abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t ov[32];
-            tmem_ld32_wait(tm_o + c, ov);
+      }
+      // pass 2: p = exp2(s * c - m) two columns at a time (packed FMA), row sum
+      // in 4 packed partial sums, P as bf16 pairs (column j = keys 2j, 2j+1).
+      // Half h reads S columns [64h, 64h + 64) and writes P columns
+      // [32h, 32h + 32); at D = 128 P sits on S's first 64 columns, which
+      // half 0 has already read.
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nsh2 = make_float2(-sh, -sh);
+      float2 s4[4];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32_wait(tm_o + c, ov);
-          }
+      for (int i = 0; i < 4; ++i) s4[i] = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[64];
+        tmem_ld64_wait(tm_s + 64 * h, sr);
+        if (lim < kBN) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (64 * h + c >= lim) sr[c] = __float_as_uint(kNegInf);
+        }
+        uint32_t pw[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                 sc2, nsh2);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          s4[(c >> 1) & 3] = fadd2(s4[(c >> 1) & 3], pp);
+          pw[c >> 1] = pack_bf16x2(pp.x, pp.y);
+        }
+        tmem_st32_wait(tm_p + 32 * h, pw);
+      }
+      const float2 st = fadd2(fadd2(s4[0], s4[1]), fadd2(s4[2], s4[3]));
+      l_run = l_run * alpha + (st.x + st.y);
+      m_run = m_use;
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32_wait(tm_o + c, ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32_wait(tm_o + c, ov);
         }
       }
-      // P (bf16) into the 128-byte-swizzled K-major tile: 16-byte piece q of
-      // row r sits at r*128 + ((q ^ (r & 7)) * 16) inside its 64-key block
-#pragma unroll
-      for (int q16 = 0; q16 < 16; ++q16) {
-        const int blk = q16 >> 3, piece = q16 & 7;
-        uint4* dst = reinterpret_cast<uint4*>(p_tile + blk * kChunk + r * 128 +
-                                              ((piece ^ (r & 7)) << 4));
-        *dst = make_uint4(pw[4 * q16], pw[4 * q16 + 1], pw[4 * q16 + 2], pw[4 * q16 + 3]);
-      }
-      fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.p_full[t]);
+      if (lane == 0) {
+        mbar_arrive(&bar.s_free[t]);
+        mbar_arrive(&bar.p_full[t]);
+      }
     }
     // epilogue: O = acc / l, LSE = (m + log2 l) ln 2
     const bool row_ok = row < p.Sq && qt < p.nqt;
@@ -522,6 +559,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
     *why = "shared memory attribute";
     return e;
   }
+
   Params p{};
   p.B = a.B; p.H = a.H; p.Hkv = a.Hkv; p.Sq = a.Sq; p.Sk = a.Sk;
   p.scale_log2 = a.scale * kLog2e;
