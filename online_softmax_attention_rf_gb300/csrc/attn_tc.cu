@@ -11,7 +11,12 @@
 // Masked 128 x 128 tiles are never visited (STOF, Méthodologie: block-sparse
 // outer tiles in row-compressed lists; skipped, not zeroed).
 //
-// CTA = two 128-row query tiles of one (batch, head), sharing one K/V stream.
+// Each CTA runs two work items back to back; an item is two 128-row query
+// tiles of one (batch, head) sharing one K/V stream, and a CTA pairs a heavy
+// and a light item of one head so causal work is even across CTAs. Tensor
+// memory, barriers and the pipeline stay live across the items, the second
+// item's Q tiles load as soon as the last QK of the first has read each, and
+// the epilogue of the first overlaps the first MMAs of the second.
 // Warp roles (320 threads):
 //   warps 0-3  softmax group 0 (query tile 0: thread r owns row r, TMEM lane r)
 //   warps 4-7  softmax group 1 (query tile 1)
@@ -85,6 +90,7 @@ struct Bars {
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t q_full[2];
+  uint64_t q_empty[2];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
@@ -188,6 +194,29 @@ __device__ __forceinline__ void issue_pv(uint32_t tm_o, uint32_t tm_p, uint32_t 
   }
 }
 
+// Work items of one CTA. An item is a pair of query tiles of one head; CTA x
+// takes two items of head x / ceil(pairs / 2): the pair counted j from the top
+// (heavy under causal masking: later tiles see more keys) and the pair counted
+// j from the bottom (light), so every CTA carries about the same causal work
+// and the hardware's CTA scheduler balances the rest. CTAs run head-major,
+// which keeps each head's K/V in L2 while its CTAs run. Returns false when
+// the CTA has no k-th item.
+__device__ __forceinline__ bool cta_item(const Params& p, int k, int& bh, int& qt0) {
+  const int half = (p.pairs + 1) / 2;
+  const int x = static_cast<int>(blockIdx.x);
+  const int j = x % half;
+  bh = x / half;
+  if (k == 0) {
+    qt0 = 2 * (p.pairs - 1 - j);
+    return true;
+  }
+  if (k == 1 && j != p.pairs - 1 - j) {
+    qt0 = 2 * j;
+    return true;
+  }
+  return false;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -201,15 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_base = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // head-major order, so that the CTAs of one head (and of the query heads
-  // that share a kv head) run together and keep its K/V in L2; within a head
-  // the heavy query-tile pairs go first (causal: later tiles see more keys)
-  const int pair = p.pairs - 1 - static_cast<int>(blockIdx.x % p.pairs);
-  const int bh = static_cast<int>(blockIdx.x / p.pairs);
-  const int b = bh / p.H, h = bh % p.H;
-  const int bk = b * p.Hkv + h / (p.H / p.Hkv);
-  const int qt0 = 2 * pair;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&bar.kv_full[i], 1);
@@ -217,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar.q_full[t], 1);
+      mbar_init(&bar.q_empty[t], 1);
       mbar_init(&bar.s_full[t], 1);
       mbar_init(&bar.s_free[t], 4);
       mbar_init(&bar.p_full[t], 4);
@@ -238,37 +259,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
+    // Per item: the first K/V pair, then Q0 and Q1 (each once the previous
+    // item's last QK on it has completed), then the remaining K/V pairs.
     if (lane == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      UnionIter it{tile_list(p, bh, qt0, false), tile_list(p, bh, qt0 + 1, false)};
-      const int bhq = bh;
-      for (int t = 0; t < 2; ++t) {
-        if ((t == 0 ? it.l0.n : it.l1.n) == 0) continue;
-        mbar_arrive_expect_tx(&bar.q_full[t], L::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::kOffQ + t * L::kTileBytes + c * kChunk, &tm_q, &bar.q_full[t],
-                      c * 64, (qt0 + t) * kBM, bhq);
-      }
-      int u;
-      bool n0, n1;
       int seq = 0;
       int last[8];
       for (int i = 0; i < NS; ++i) last[i] = -1;
+      int q_loads[2] = {0, 0};
       bool ok = true;
-      while (ok && it.next(u, n0, n1)) {
-        for (int kv = 0; kv < 2 && ok; ++kv, ++seq) {
-          const int slot = seq % NS;
-          ok = mbar_wait(&bar.kv_empty[slot], ((seq / NS) & 1) ^ 1, p.status,
-                         dev_code(kDevTimeout, kKerAttnTc, 10), abort_flag);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&bar.kv_full[slot], L::kTileBytes);
-          unsigned char* dst = smem + L::kOffKV + slot * L::kTileBytes;
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(dst + c * kChunk, kv == 0 ? &tm_k : &tm_v, &bar.kv_full[slot], c * 64,
-                        u * kBN, bk);
-          last[slot] = seq;
+      int bh, qt0;
+      for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
+        const int bk = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);
+        UnionIter it{tile_list(p, bh, qt0, false), tile_list(p, bh, qt0 + 1, false)};
+        const int nt[2] = {it.l0.n, it.l1.n};
+        int u;
+        bool n0, n1;
+        bool first = true;
+        while (ok && it.next(u, n0, n1)) {
+          for (int kv = 0; kv < 2 && ok; ++kv, ++seq) {
+            const int slot = seq % NS;
+            ok = mbar_wait(&bar.kv_empty[slot], ((seq / NS) & 1) ^ 1, p.status,
+                           dev_code(kDevTimeout, kKerAttnTc, 10), abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bar.kv_full[slot], L::kTileBytes);
+            unsigned char* dst = smem + L::kOffKV + slot * L::kTileBytes;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(dst + c * kChunk, kv == 0 ? &tm_k : &tm_v, &bar.kv_full[slot], c * 64,
+                          u * kBN, bk);
+            last[slot] = seq;
+          }
+          if (first && ok) {
+            first = false;
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (nt[t] == 0) continue;
+              if (q_loads[t] > 0)
+                ok = mbar_wait(&bar.q_empty[t], (q_loads[t] - 1) & 1, p.status,
+                               dev_code(kDevTimeout, kKerAttnTc, 12), abort_flag);
+              if (!ok) break;
+              mbar_arrive_expect_tx(&bar.q_full[t], L::kTileBytes);
+              for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(smem + L::kOffQ + t * L::kTileBytes + c * kChunk, &tm_q,
+                            &bar.q_full[t], c * 64, (qt0 + t) * kBM, bh);
+              ++q_loads[t];
+            }
+          }
         }
       }
       // never leave with copies in flight
@@ -276,6 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last[i] >= 0)
           mbar_wait(&bar.kv_full[i], (last[i] / NS) & 1, p.status,
                     dev_code(kDevTimeout, kKerAttnTc, 11), nullptr);
+      for (int t = 0; t < 2; ++t)
+        if (q_loads[t] > 0)
+          mbar_wait(&bar.q_full[t], (q_loads[t] - 1) & 1, p.status,
+                    dev_code(kDevTimeout, kKerAttnTc, 13), nullptr);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -284,72 +325,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   QK0(u), PV1(u'), QK1(u), PV0(u)
     // so each softmax group has about two MMAs of slack between its S being
     // ready and its P being consumed, and K/V slots are released as early as
-    // their last reader is issued (commit-tracked).
+    // their last reader is issued (commit-tracked). After the last QK of a
+    // query tile in an item, its Q buffer is released for the next item.
     if (lane == 0) {
-      UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, true)};
       const uint32_t q_s[2] = {s_base + L::kOffQ, s_base + L::kOffQ + L::kTileBytes};
       const uint32_t tm_p[2] = {tmem + L::tmem_p(0), tmem + L::tmem_p(1)};
       const uint32_t tm_s[2] = {tmem + L::kTmemS, tmem + L::kTmemS + kBN};
       const uint32_t tm_o[2] = {tmem + L::kTmemO, tmem + L::kTmemO + D};
-      int nq[2] = {0, 0};    // QK tiles issued per query tile
-      int npv[2] = {0, 0};   // PV tiles issued per query tile
-      bool q_ready[2] = {false, false};
+      int nq[2] = {0, 0};      // QK tiles issued per query tile (all items)
+      int npv[2] = {0, 0};     // PV tiles issued per query tile (all items)
+      int q_uses[2] = {0, 0};  // items whose Q_t has been consumed
       bool issued_any = false;
-      int pend1 = -1;        // load sequence number of the V tile query tile 1 still owes
       int seq = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bb, int parity, int site) {
         return mbar_wait(bb, parity, p.status, dev_code(kDevTimeout, kKerAttnTc, site), abort_flag);
       };
       auto slot_addr = [&](int sq) { return s_base + L::kOffKV + (sq % NS) * L::kTileBytes; };
-      auto qk = [&](int t, int kseq, int u) -> bool {
-        if (!q_ready[t]) {
-          if (!wait(&bar.q_full[t], 0, 22)) return false;
-          q_ready[t] = true;
-        }
-        if (nq[t] > 0) {
-          if (!wait(&bar.s_free[t], (nq[t] - 1) & 1, 23)) return false;
+      int bh, qt0;
+      for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
+        UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, true)};
+        bool q_ready[2] = {false, false};
+        int pv_item[2] = {0, 0};   // PV tiles of this item per query tile
+        int pend1 = -1;            // V load sequence number query tile 1 still owes a PV
+        auto qk = [&](int t, int kseq, int u) -> bool {
+          if (!q_ready[t]) {
+            if (!wait(&bar.q_full[t], q_uses[t] & 1, 22)) return false;
+            q_ready[t] = true;
+          }
+          if (nq[t] > 0) {
+            if (!wait(&bar.s_free[t], (nq[t] - 1) & 1, 23)) return false;
+            tc_fence_after_sync();
+          }
+          issue_qk<D>(tm_s[t], q_s[t], slot_addr(kseq));
+          mma_commit(&bar.s_full[t]);
+          issued_any = true;
+          ++nq[t];
+          if (p.visited != nullptr) p.visited[(int64_t(bh) * p.nqt + qt0 + t) * p.nkt + u] = 1;
+          // last QK of this query tile in the item: release Q_t
+          if ((t == 0 ? it.i0 == it.l0.n : it.i1 == it.l1.n)) {
+            mma_commit(&bar.q_empty[t]);
+            ++q_uses[t];
+          }
+          return true;
+        };
+        auto pv = [&](int t, int vseq) -> bool {
+          if (!wait(&bar.kv_full[vseq % NS], (vseq / NS) & 1, 24)) return false;
+          if (!wait(&bar.p_full[t], npv[t] & 1, 25)) return false;
           tc_fence_after_sync();
+          issue_pv<D>(tm_o[t], tm_p[t], slot_addr(vseq), pv_item[t] > 0);
+          mma_commit(&bar.o_done[t]);
+          ++npv[t];
+          ++pv_item[t];
+          return true;
+        };
+        int u;
+        bool need0, need1;
+        while (ok && it.next(u, need0, need1)) {
+          const int kseq = seq, vseq = seq + 1;
+          seq += 2;
+          ok = wait(&bar.kv_full[kseq % NS], (kseq / NS) & 1, 21);
+          if (!ok) break;
+          tc_fence_after_sync();
+          if (need0 && !(ok = qk(0, kseq, u))) break;
+          if (pend1 >= 0) {
+            if (!(ok = pv(1, pend1))) break;
+            mma_commit(&bar.kv_empty[pend1 % NS]);
+            pend1 = -1;
+          }
+          if (need1 && !(ok = qk(1, kseq, u))) break;
+          mma_commit(&bar.kv_empty[kseq % NS]);
+          if (need0 && !(ok = pv(0, vseq))) break;
+          if (need1)
+            pend1 = vseq;
+          else
+            mma_commit(&bar.kv_empty[vseq % NS]);
         }
-        issue_qk<D>(tm_s[t], q_s[t], slot_addr(kseq));
-        mma_commit(&bar.s_full[t]);
-        issued_any = true;
-        ++nq[t];
-        if (p.visited != nullptr) p.visited[(int64_t(bh) * p.nqt + qt0 + t) * p.nkt + u] = 1;
-        return true;
-      };
-      auto pv = [&](int t, int vseq) -> bool {
-        if (!wait(&bar.kv_full[vseq % NS], (vseq / NS) & 1, 24)) return false;
-        if (!wait(&bar.p_full[t], npv[t] & 1, 25)) return false;
-        tc_fence_after_sync();
-        issue_pv<D>(tm_o[t], tm_p[t], slot_addr(vseq), npv[t] > 0);
-        mma_commit(&bar.o_done[t]);
-        ++npv[t];
-        return true;
-      };
-      int u;
-      bool need0, need1;
-      while (ok && it.next(u, need0, need1)) {
-        const int kseq = seq, vseq = seq + 1;
-        seq += 2;
-        ok = wait(&bar.kv_full[kseq % NS], (kseq / NS) & 1, 21);
-        if (!ok) break;
-        tc_fence_after_sync();
-        if (need0 && !(ok = qk(0, kseq, u))) break;
-        if (pend1 >= 0) {
-          if (!(ok = pv(1, pend1))) break;
-          mma_commit(&bar.kv_empty[pend1 % NS]);
-          pend1 = -1;
-        }
-        if (need1 && !(ok = qk(1, kseq, u))) break;
-        mma_commit(&bar.kv_empty[kseq % NS]);
-        if (need0 && !(ok = pv(0, vseq))) break;
-        if (need1)
-          pend1 = vseq;
-        else
-          mma_commit(&bar.kv_empty[vseq % NS]);
+        if (ok && pend1 >= 0 && (ok = pv(1, pend1))) mma_commit(&bar.kv_empty[pend1 % NS]);
       }
-      if (ok && pend1 >= 0 && (ok = pv(1, pend1))) mma_commit(&bar.kv_empty[pend1 % NS]);
       // never leave with MMAs in flight (their operands live in this CTA)
       if (issued_any) {
         mma_commit(&bar.mma_idle);
@@ -362,121 +415,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;             // query tile of this group
     const int r = threadIdx.x & 127;     // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int qt = qt0 + t;
-    const int64_t row = int64_t(qt) * kBM + r;
-    const TileList list = tile_list(p, bh, qt, false);
     const uint32_t tm_s = tmem + L::kTmemS + t * kBN + lane_off;
     const uint32_t tm_o = tmem + L::kTmemO + t * D + lane_off;
     const uint32_t tm_p = tmem + L::tmem_p(t) + lane_off;
     const int64_t shift = int64_t(p.Sk) - p.Sq;
-    const int64_t row_lim = p.causal ? min64(p.Sk, row + 1 + shift) : p.Sk;
-    const int64_t tile_first_lim =
-        p.causal ? min64(p.Sk, int64_t(qt) * kBM + 1 + shift) : p.Sk;
-    float m_run = kNegInf, l_run = 0.f;
+    int j = 0;                           // S tiles consumed (all items)
     bool ok = true;
-    for (int j = 0; j < list.n && ok; ++j) {
-      const int u = list.at(j);
-      ok = mbar_wait_warp(&bar.s_full[t], j & 1, p.status, dev_code(kDevTimeout, kKerAttnTc, 30),
-                          abort_flag);
-      if (!ok) break;
-      tc_fence_after_sync();
-      // element mask only where the tile crosses the causal diagonal or Sk
-      const int64_t k0 = int64_t(u) * kBN;
-      const int lim = (k0 + kBN > tile_first_lim)
-                          ? static_cast<int>(max64(int64_t(0), min64(kBN, row_lim - k0)))
-                          : kBN;
-      // pass 1: row maximum over all 128 columns (one TMEM read), 8
-      // independent partial maxima, two columns per step (max is exact, so
-      // the order does not matter)
-      float mx;
-      {
-        uint32_t sr[128];
-        tmem_ld128_wait(tm_s, sr);
-        if (lim < kBN) {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c >= lim) sr[c] = __float_as_uint(kNegInf);
-        }
-        float m8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = kNegInf;
-#pragma unroll
-        for (int c = 0; c < kBN; c += 2)
-          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sr[c]),
-                                   __uint_as_float(sr[c + 1]));
-        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-      }
-      const float m_new = (mx == kNegInf) ? m_run : fmaxf(m_run, mx * p.scale_log2);
-      const bool resc = m_new > m_run + kRescaleThreshold;
-      const float m_use = resc ? m_new : m_run;
-      const float alpha = resc ? ex2_approx(m_run - m_new) : 1.f;
-      const float sh = (m_use == kNegInf) ? 0.f : m_use;
-      if (j > 0) {
-        // the previous P.V must be done before P_t's columns are rewritten and
-        // O_t is rescaled (it was issued before the QK that produced this S,
-        // so this wait normally returns at once)
-        ok = mbar_wait_warp(&bar.o_done[t], (j - 1) & 1, p.status,
-                            dev_code(kDevTimeout, kKerAttnTc, 31), abort_flag);
+    int bh, qt0;
+    for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
+      const int qt = qt0 + t;
+      const int64_t row = int64_t(qt) * kBM + r;
+      const TileList list = tile_list(p, bh, qt, false);
+      const int64_t row_lim = p.causal ? min64(p.Sk, row + 1 + shift) : p.Sk;
+      const int64_t tile_first_lim =
+          p.causal ? min64(p.Sk, int64_t(qt) * kBM + 1 + shift) : p.Sk;
+      float m_run = kNegInf, l_run = 0.f;
+      for (int jj = 0; jj < list.n && ok; ++jj, ++j) {
+        const int u = list.at(jj);
+        ok = mbar_wait_warp(&bar.s_full[t], j & 1, p.status,
+                            dev_code(kDevTimeout, kKerAttnTc, 30), abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
-      }
-      // pass 2: p = exp2(s * c - m) two columns at a time (packed FMA), row sum
-      // in 4 packed partial sums, P as bf16 pairs (column j = keys 2j, 2j+1).
-      // Half h reads S columns [64h, 64h + 64) and writes P columns
-      // [32h, 32h + 32); at D = 128 P sits on S's first 64 columns, which
-      // half 0 has already read.
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-      const float2 nsh2 = make_float2(-sh, -sh);
-      float2 s4[4];
+        // element mask only where the tile crosses the causal diagonal or Sk
+        const int64_t k0 = int64_t(u) * kBN;
+        const int lim = (k0 + kBN > tile_first_lim)
+                            ? static_cast<int>(max64(int64_t(0), min64(kBN, row_lim - k0)))
+                            : kBN;
+        // pass 1: row maximum over all 128 columns (one TMEM read), 8
+        // independent partial maxima, two columns per step (max is exact, so
+        // the order does not matter)
+        float mx;
+        {
+          uint32_t sr[128];
+          tmem_ld128_wait(tm_s, sr);
+          if (lim < kBN) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) s4[i] = make_float2(0.f, 0.f);
+            for (int c = 0; c < kBN; ++c)
+              if (c >= lim) sr[c] = __float_as_uint(kNegInf);
+          }
+          float m8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = kNegInf;
+#pragma unroll
+          for (int c = 0; c < kBN; c += 2)
+            m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sr[c]),
+                                     __uint_as_float(sr[c + 1]));
+          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                     fmaxf(m8[6], m8[7]));
+        }
+        const float m_new = (mx == kNegInf) ? m_run : fmaxf(m_run, mx * p.scale_log2);
+        const bool resc = m_new > m_run + kRescaleThreshold;
+        const float m_use = resc ? m_new : m_run;
+        const float alpha = resc ? ex2_approx(m_run - m_new) : 1.f;
+        const float sh = (m_use == kNegInf) ? 0.f : m_use;
+        if (jj > 0) {
+          // the previous P.V must be done before P_t's columns are rewritten
+          // and O_t is rescaled (it was issued before the QK that produced
+          // this S, so this wait normally returns at once)
+          ok = mbar_wait_warp(&bar.o_done[t], (j - 1) & 1, p.status,
+                              dev_code(kDevTimeout, kKerAttnTc, 31), abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
+        // pass 2: p = exp2(s * c - m) two columns at a time (packed FMA), row
+        // sum in 4 packed partial sums, P as bf16 pairs (column j = keys 2j,
+        // 2j+1). Half h reads S columns [64h, 64h + 64) and writes P columns
+        // [32h, 32h + 32); at D = 128 P sits on S's first 64 columns, which
+        // half 0 has already read.
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nsh2 = make_float2(-sh, -sh);
+        float2 s4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s4[i] = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sr[64];
-        tmem_ld64_wait(tm_s + 64 * h, sr);
-        if (lim < kBN) {
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sr[64];
+          tmem_ld64_wait(tm_s + 64 * h, sr);
+          if (lim < kBN) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (64 * h + c >= lim) sr[c] = __float_as_uint(kNegInf);
-        }
-        uint32_t pw[32];
+            for (int c = 0; c < 64; ++c)
+              if (64 * h + c >= lim) sr[c] = __float_as_uint(kNegInf);
+          }
+          uint32_t pw[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float2 x = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
-                                 sc2, nsh2);
-          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          s4[(c >> 1) & 3] = fadd2(s4[(c >> 1) & 3], pp);
-          pw[c >> 1] = pack_bf16x2(pp.x, pp.y);
+          for (int c = 0; c < 64; c += 2) {
+            const float2 x = ffma2(
+                make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nsh2);
+            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            s4[(c >> 1) & 3] = fadd2(s4[(c >> 1) & 3], pp);
+            pw[c >> 1] = pack_bf16x2(pp.x, pp.y);
+          }
+          tmem_st32(tm_p + 32 * h, pw);
         }
-        tmem_st32_wait(tm_p + 32 * h, pw);
-      }
-      const float2 st = fadd2(fadd2(s4[0], s4[1]), fadd2(s4[2], s4[3]));
-      l_run = l_run * alpha + (st.x + st.y);
-      m_run = m_use;
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        tmem_wait_st();
+        const float2 st = fadd2(fadd2(s4[0], s4[1]), fadd2(s4[2], s4[3]));
+        l_run = l_run * alpha + (st.x + st.y);
+        m_run = m_use;
+        if (jj > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32_wait(tm_o + c, ov);
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            tmem_ld32_wait(tm_o + c, ov);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32_wait(tm_o + c, ov);
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32_wait(tm_o + c, ov);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar.s_free[t]);
+          mbar_arrive(&bar.p_full[t]);
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bar.s_free[t]);
-        mbar_arrive(&bar.p_full[t]);
-      }
-    }
-    // epilogue: O = acc / l, LSE = (m + log2 l) ln 2
-    const bool row_ok = row < p.Sq && qt < p.nqt;
-    __nv_bfloat16* og = p.o + (int64_t(bh) * p.Sq + row) * D;
-    if (ok && list.n > 0) {
-      ok = mbar_wait_warp(&bar.o_done[t], (list.n - 1) & 1, p.status,
-                          dev_code(kDevTimeout, kKerAttnTc, 32), abort_flag);
-      if (ok) {
+      if (!ok) break;
+      // epilogue: O = acc / l, LSE = (m + log2 l) ln 2. The next item's first
+      // P.V on O_t is issued only after this group's next P arrives, i.e.
+      // after the TMEM reads below.
+      const bool row_ok = row < p.Sq && qt < p.nqt;
+      __nv_bfloat16* og = p.o + (int64_t(bh) * p.Sq + row) * D;
+      if (list.n > 0) {
+        ok = mbar_wait_warp(&bar.o_done[t], (j - 1) & 1, p.status,
+                            dev_code(kDevTimeout, kKerAttnTc, 32), abort_flag);
+        if (!ok) break;
         tc_fence_after_sync();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
@@ -495,14 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        tc_fence_before_sync();
         if (row_ok && p.lse != nullptr)
-          p.lse[int64_t(bh) * p.Sq + row] =
-              l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : kNegInf;
+          p.lse[int64_t(bh) * p.Sq + row] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : kNegInf;
+      } else if (row_ok) {
+        // no visible key for any row of this tile
+        for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(og + c) = make_uint4(0, 0, 0, 0);
+        if (p.lse != nullptr) p.lse[int64_t(bh) * p.Sq + row] = kNegInf;
       }
-    } else if (ok && row_ok) {
-      // no visible key for any row of this tile
-      for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(og + c) = make_uint4(0, 0, 0, 0);
-      if (p.lse != nullptr) p.lse[int64_t(bh) * p.Sq + row] = kNegInf;
     }
   }
 
@@ -571,11 +632,13 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
   p.lse = a.lse;
   p.visited = a.visited;
   p.status = a.status;
-  const int64_t grid = int64_t(p.pairs) * a.B * a.H;
-  if (grid > 0x7fffffffLL) {
-    *why = "grid too large";
+  const int64_t items = int64_t(p.pairs) * a.B * a.H;
+  if (items > 0x7fffffffLL) {
+    *why = "too many work items";
     return cudaErrorInvalidConfiguration;
   }
+  // two items (a heavy and a light query-tile pair of one head) per CTA
+  const int64_t grid = int64_t((p.pairs + 1) / 2) * a.B * a.H;
   attn_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
