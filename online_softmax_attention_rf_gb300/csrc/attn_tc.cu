@@ -92,7 +92,6 @@ struct Bars {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
-  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t mma_idle;
@@ -170,27 +169,29 @@ struct UnionIter {
   }
 };
 
+// Shared-memory descriptors are built once; an MMA step only adds a constant
+// offset (in 16-byte units) to the start-address field, which cannot carry
+// out of its 14 bits because shared memory ends below 256 KB.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tm_s, uint32_t q_s, uint32_t k_s) {
+__device__ __forceinline__ void issue_qk(uint32_t tm_s, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-    mma_bf16(tm_s, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024), idesc,
-             kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kChunk + (kk & 3) * 32) >> 4);
+    mma_bf16(tm_s, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 // O_t (+)= P_t V: A = P_t from tensor memory (8 columns per 16 keys),
 // B = V from shared memory as an MN-major operand.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tm_o, uint32_t tm_p, uint32_t v_s,
+__device__ __forceinline__ void issue_pv(uint32_t tm_o, uint32_t tm_p, uint64_t v_desc,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 1);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    const uint64_t b = sdesc_sw128(v_s + kk * 16 * 128, kChunk, 1024);
-    mma_bf16_ts(tm_o, tm_p + kk * 8, b, idesc, (kk > 0 || accumulate) ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+    mma_bf16_ts(tm_o, tm_p + kk * 8, v_desc + off, idesc, (kk > 0 || accumulate) ? 1u : 0u);
   }
 }
 
@@ -239,7 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.q_full[t], 1);
       mbar_init(&bar.q_empty[t], 1);
       mbar_init(&bar.s_full[t], 1);
-      mbar_init(&bar.s_free[t], 4);
       mbar_init(&bar.p_full[t], 4);
       mbar_init(&bar.o_done[t], 1);
     }
@@ -327,82 +327,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ready and its P being consumed, and K/V slots are released as early as
     // their last reader is issued (commit-tracked). After the last QK of a
     // query tile in an item, its Q buffer is released for the next item.
+    // The tensor pipe buffers only a few MMAs, so this lane keeps the work
+    // between issue blocks minimal: QK_t(u+1) needs no wait of its own,
+    // because it is issued after PV_t(u), which waited for the softmax to have
+    // read S_t(u) and written P_t(u).
     if (lane == 0) {
-      const uint32_t q_s[2] = {s_base + L::kOffQ, s_base + L::kOffQ + L::kTileBytes};
-      const uint32_t tm_p[2] = {tmem + L::tmem_p(0), tmem + L::tmem_p(1)};
-      const uint32_t tm_s[2] = {tmem + L::kTmemS, tmem + L::kTmemS + kBN};
-      const uint32_t tm_o[2] = {tmem + L::kTmemO, tmem + L::kTmemO + D};
-      int nq[2] = {0, 0};      // QK tiles issued per query tile (all items)
-      int npv[2] = {0, 0};     // PV tiles issued per query tile (all items)
-      int q_uses[2] = {0, 0};  // items whose Q_t has been consumed
+      const uint64_t q_desc0 = sdesc_sw128(s_base + L::kOffQ, 16, 1024);
+      const uint64_t q_desc1 = sdesc_sw128(s_base + L::kOffQ + L::kTileBytes, 16, 1024);
+      // K slots are K-major operands, V slots MN-major (64-column blocks
+      // kChunk bytes apart); slot s starts s * kTileBytes after slot 0
+      const uint64_t k_desc0 = sdesc_sw128(s_base + L::kOffKV, 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(s_base + L::kOffKV, kChunk, 1024);
+      const uint32_t tm_s0 = tmem + L::kTmemS, tm_s1 = tmem + L::kTmemS + kBN;
+      const uint32_t tm_o0 = tmem + L::kTmemO, tm_o1 = tmem + L::kTmemO + D;
+      const uint32_t tm_p0 = tmem + L::tmem_p(0), tm_p1 = tmem + L::tmem_p(1);
+      int npv0 = 0, npv1 = 0;        // PV tiles issued per query tile (all items)
+      int qu0 = 0, qu1 = 0;          // items whose Q tile has been consumed
       bool issued_any = false;
       int seq = 0;
       bool ok = true;
-      auto wait = [&](uint64_t* bb, int parity, int site) {
-        return mbar_wait(bb, parity, p.status, dev_code(kDevTimeout, kKerAttnTc, site), abort_flag);
-      };
-      auto slot_addr = [&](int sq) { return s_base + L::kOffKV + (sq % NS) * L::kTileBytes; };
+#define RF_WAIT(b, par, site)                                                        \
+  mbar_wait(&bar.b, (par), p.status, dev_code(kDevTimeout, kKerAttnTc, site), abort_flag)
+#define RF_SLOT(sq) (static_cast<uint64_t>((((sq) % NS) * L::kTileBytes) >> 4))
       int bh, qt0;
       for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
         UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, true)};
-        bool q_ready[2] = {false, false};
-        int pv_item[2] = {0, 0};   // PV tiles of this item per query tile
-        int pend1 = -1;            // V load sequence number query tile 1 still owes a PV
-        auto qk = [&](int t, int kseq, int u) -> bool {
-          if (!q_ready[t]) {
-            if (!wait(&bar.q_full[t], q_uses[t] & 1, 22)) return false;
-            q_ready[t] = true;
-          }
-          if (nq[t] > 0) {
-            if (!wait(&bar.s_free[t], (nq[t] - 1) & 1, 23)) return false;
-            tc_fence_after_sync();
-          }
-          issue_qk<D>(tm_s[t], q_s[t], slot_addr(kseq));
-          mma_commit(&bar.s_full[t]);
-          issued_any = true;
-          ++nq[t];
-          if (p.visited != nullptr) p.visited[(int64_t(bh) * p.nqt + qt0 + t) * p.nkt + u] = 1;
-          // last QK of this query tile in the item: release Q_t
-          if ((t == 0 ? it.i0 == it.l0.n : it.i1 == it.l1.n)) {
-            mma_commit(&bar.q_empty[t]);
-            ++q_uses[t];
-          }
-          return true;
-        };
-        auto pv = [&](int t, int vseq) -> bool {
-          if (!wait(&bar.kv_full[vseq % NS], (vseq / NS) & 1, 24)) return false;
-          if (!wait(&bar.p_full[t], npv[t] & 1, 25)) return false;
-          tc_fence_after_sync();
-          issue_pv<D>(tm_o[t], tm_p[t], slot_addr(vseq), pv_item[t] > 0);
-          mma_commit(&bar.o_done[t]);
-          ++npv[t];
-          ++pv_item[t];
-          return true;
-        };
+        bool qr0 = false, qr1 = false;   // Q tile present for this item
+        bool acc0 = false, acc1 = false; // O_t holds this item's partial sum
+        int pend1 = -1;                  // V load sequence number tile 1 still owes
         int u;
         bool need0, need1;
-        while (ok && it.next(u, need0, need1)) {
+        while (it.next(u, need0, need1)) {
           const int kseq = seq, vseq = seq + 1;
           seq += 2;
-          ok = wait(&bar.kv_full[kseq % NS], (kseq / NS) & 1, 21);
-          if (!ok) break;
-          tc_fence_after_sync();
-          if (need0 && !(ok = qk(0, kseq, u))) break;
+          if (!(ok = RF_WAIT(kv_full[kseq % NS], (kseq / NS) & 1, 21))) break;
+          const uint64_t kd = k_desc0 + RF_SLOT(kseq);
+          if (need0) {
+            if (!qr0) {
+              if (!(ok = RF_WAIT(q_full[0], qu0 & 1, 22))) break;
+              qr0 = true;
+            }
+            issue_qk<D>(tm_s0, q_desc0, kd);
+            mma_commit(&bar.s_full[0]);
+            issued_any = true;
+            if (it.i0 == it.l0.n) {  // last QK on Q0 in this item
+              mma_commit(&bar.q_empty[0]);
+              ++qu0;
+            }
+            if (p.visited != nullptr) p.visited[(int64_t(bh) * p.nqt + qt0) * p.nkt + u] = 1;
+          }
           if (pend1 >= 0) {
-            if (!(ok = pv(1, pend1))) break;
+            if (!(ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 24))) break;
+            if (!(ok = RF_WAIT(p_full[1], npv1 & 1, 25))) break;
+            tc_fence_after_sync();
+            issue_pv<D>(tm_o1, tm_p1, v_desc0 + RF_SLOT(pend1), acc1);
+            acc1 = true;
+            ++npv1;
+            mma_commit(&bar.o_done[1]);
             mma_commit(&bar.kv_empty[pend1 % NS]);
             pend1 = -1;
           }
-          if (need1 && !(ok = qk(1, kseq, u))) break;
+          if (need1) {
+            if (!qr1) {
+              if (!(ok = RF_WAIT(q_full[1], qu1 & 1, 22))) break;
+              qr1 = true;
+            }
+            issue_qk<D>(tm_s1, q_desc1, kd);
+            mma_commit(&bar.s_full[1]);
+            issued_any = true;
+            if (it.i1 == it.l1.n) {
+              mma_commit(&bar.q_empty[1]);
+              ++qu1;
+            }
+            if (p.visited != nullptr)
+              p.visited[(int64_t(bh) * p.nqt + qt0 + 1) * p.nkt + u] = 1;
+          }
           mma_commit(&bar.kv_empty[kseq % NS]);
-          if (need0 && !(ok = pv(0, vseq))) break;
+          if (need0) {
+            if (!(ok = RF_WAIT(kv_full[vseq % NS], (vseq / NS) & 1, 24))) break;
+            if (!(ok = RF_WAIT(p_full[0], npv0 & 1, 25))) break;
+            tc_fence_after_sync();
+            issue_pv<D>(tm_o0, tm_p0, v_desc0 + RF_SLOT(vseq), acc0);
+            acc0 = true;
+            ++npv0;
+            mma_commit(&bar.o_done[0]);
+          }
           if (need1)
             pend1 = vseq;
           else
             mma_commit(&bar.kv_empty[vseq % NS]);
         }
-        if (ok && pend1 >= 0 && (ok = pv(1, pend1))) mma_commit(&bar.kv_empty[pend1 % NS]);
+        if (ok && pend1 >= 0) {
+          if ((ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 26)) &&
+              (ok = RF_WAIT(p_full[1], npv1 & 1, 27))) {
+            tc_fence_after_sync();
+            issue_pv<D>(tm_o1, tm_p1, v_desc0 + RF_SLOT(pend1), acc1);
+            ++npv1;
+            mma_commit(&bar.o_done[1]);
+            mma_commit(&bar.kv_empty[pend1 % NS]);
+          }
+        }
       }
+#undef RF_WAIT
+#undef RF_SLOT
       // never leave with MMAs in flight (their operands live in this CTA)
       if (issued_any) {
         mma_commit(&bar.mma_idle);
@@ -523,10 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bar.s_free[t]);
-          mbar_arrive(&bar.p_full[t]);
-        }
+        if (lane == 0) mbar_arrive(&bar.p_full[t]);
       }
       if (!ok) break;
       // epilogue: O = acc / l, LSE = (m + log2 l) ln 2. The next item's first

@@ -92,6 +92,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Non-blocking test for completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Test for completion of the phase with the given parity. A thread whose
 // phase is not complete is suspended until it completes or kSuspendNs pass,
 // so waiting warps do not take issue slots from working ones.
@@ -114,7 +127,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // role), records `code` and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code,
                                           volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // a phase that has already completed costs one cheap test
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -129,6 +143,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 // Whole-warp bounded wait; the result is the same in every lane.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status,
                                                int code, volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
   uint64_t t0 = 0;
   bool started = false;
   while (true) {
