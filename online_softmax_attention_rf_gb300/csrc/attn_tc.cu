@@ -330,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The tensor pipe buffers only a few MMAs, so this lane keeps the work
     // between issue blocks minimal: QK_t(u+1) needs no wait of its own,
     // because it is issued after PV_t(u), which waited for the softmax to have
-    // read S_t(u) and written P_t(u).
+    // read S_t(u) and written P_t(u). The commit that signals S_t(u+1) tracks
+    // every earlier MMA of this lane, PV_t(u) included, so the softmax needs
+    // no separate "P.V done" signal except after an item's last P.V.
     if (lane == 0) {
       const uint64_t q_desc0 = sdesc_sw128(s_base + L::kOffQ, 16, 1024);
       const uint64_t q_desc1 = sdesc_sw128(s_base + L::kOffQ + L::kTileBytes, 16, 1024);
@@ -355,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool qr0 = false, qr1 = false;   // Q tile present for this item
         bool acc0 = false, acc1 = false; // O_t holds this item's partial sum
         int pend1 = -1;                  // V load sequence number tile 1 still owes
+        bool pend1_v_ready = false;
         int u;
         bool need0, need1;
         while (it.next(u, need0, need1)) {
@@ -377,13 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.visited != nullptr) p.visited[(int64_t(bh) * p.nqt + qt0) * p.nkt + u] = 1;
           }
           if (pend1 >= 0) {
-            if (!(ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 24))) break;
+            if (!pend1_v_ready && !(ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 24))) break;
             if (!(ok = RF_WAIT(p_full[1], npv1 & 1, 25))) break;
             tc_fence_after_sync();
             issue_pv<D>(tm_o1, tm_p1, v_desc0 + RF_SLOT(pend1), acc1);
             acc1 = true;
             ++npv1;
-            mma_commit(&bar.o_done[1]);
+            if (!need1 && it.i1 == it.l1.n) mma_commit(&bar.o_done[1]);  // item's last on O1
             mma_commit(&bar.kv_empty[pend1 % NS]);
             pend1 = -1;
           }
@@ -410,15 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_pv<D>(tm_o0, tm_p0, v_desc0 + RF_SLOT(vseq), acc0);
             acc0 = true;
             ++npv0;
-            mma_commit(&bar.o_done[0]);
+            if (it.i0 == it.l0.n) mma_commit(&bar.o_done[0]);  // item's last P.V on O0
           }
-          if (need1)
+          if (need1) {
             pend1 = vseq;
-          else
+            pend1_v_ready = need0;  // PV0 has already waited for this V tile
+          } else {
             mma_commit(&bar.kv_empty[vseq % NS]);
+          }
         }
         if (ok && pend1 >= 0) {
-          if ((ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 26)) &&
+          if ((pend1_v_ready || (ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 26))) &&
               (ok = RF_WAIT(p_full[1], npv1 & 1, 27))) {
             tc_fence_after_sync();
             issue_pv<D>(tm_o1, tm_p1, v_desc0 + RF_SLOT(pend1), acc1);
@@ -447,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tm_p = tmem + L::tmem_p(t) + lane_off;
     const int64_t shift = int64_t(p.Sk) - p.Sq;
     int j = 0;                           // S tiles consumed (all items)
+    int o_items = 0;                     // items whose final P.V was waited for
     bool ok = true;
     int bh, qt0;
     for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
@@ -495,15 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_use = resc ? m_new : m_run;
         const float alpha = resc ? ex2_approx(m_run - m_new) : 1.f;
         const float sh = (m_use == kNegInf) ? 0.f : m_use;
-        if (jj > 0) {
-          // the previous P.V must be done before P_t's columns are rewritten
-          // and O_t is rescaled (it was issued before the QK that produced
-          // this S, so this wait normally returns at once)
-          ok = mbar_wait_warp(&bar.o_done[t], (j - 1) & 1, p.status,
-                              dev_code(kDevTimeout, kKerAttnTc, 31), abort_flag);
-          if (!ok) break;
-          tc_fence_after_sync();
-        }
+        // (the previous P.V on O_t and P_t has completed: the commit that
+        // signalled this S tracks it)
         // pass 2: p = exp2(s * c - m) two columns at a time (packed FMA), row
         // sum in 4 packed partial sums, P as bf16 pairs (column j = keys 2j,
         // 2j+1). Half h reads S columns [64h, 64h + 64) and writes P columns
@@ -559,8 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = row < p.Sq && qt < p.nqt;
       __nv_bfloat16* og = p.o + (int64_t(bh) * p.Sq + row) * D;
       if (list.n > 0) {
-        ok = mbar_wait_warp(&bar.o_done[t], (j - 1) & 1, p.status,
+        ok = mbar_wait_warp(&bar.o_done[t], o_items & 1, p.status,
                             dev_code(kDevTimeout, kKerAttnTc, 32), abort_flag);
+        ++o_items;
         if (!ok) break;
         tc_fence_after_sync();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
