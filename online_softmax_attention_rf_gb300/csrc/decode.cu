@@ -82,6 +82,20 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xffff0000u);
 }
 
+// This lane's D/32 elements of a bf16 row as D/64 packed float pairs.
+template <int D>
+__device__ __forceinline__ void load_row_pairs(const __nv_bfloat16* row, float2 (&out)[D / 64]) {
+  const int lane = threadIdx.x & 31;
+  if constexpr (D == 128) {
+    const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 4);
+    bf16x2_to_f32(w.x, out[0].x, out[0].y);
+    bf16x2_to_f32(w.y, out[1].x, out[1].y);
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 2);
+    bf16x2_to_f32(w, out[0].x, out[0].y);
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void load_row_slice(const __nv_bfloat16* row, float (&out)[D / 32]) {
   const int lane = threadIdx.x & 31;
@@ -178,12 +192,19 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
   }
   // state: running max per head (all lanes), lane-partial sums for the two
   // heads this lane scores, accumulators [head][own head-dim slice]
-  float m[GP], lpart[2] = {0.f, 0.f}, acc[GP][DPL];
+  constexpr int DP2 = DPL / 2;  // packed float pairs per lane
+  float2 q2[GP][DP2];
+#pragma unroll
+  for (int g = 0; g < GP; ++g)
+#pragma unroll
+    for (int e = 0; e < DP2; ++e) q2[g][e] = make_float2(qv[g][2 * e], qv[g][2 * e + 1]);
+  float m[GP], lpart[2] = {0.f, 0.f};
+  float2 acc[GP][DP2];
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
     m[g] = kNegInf;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
+    for (int e = 0; e < DP2; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
   // this lane's two scores are (key 2l/GP, head 2l%GP) and (.., +1)
   const int my_key = (2 * lane) / GP;
@@ -205,14 +226,14 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
       float part[64];
 #pragma unroll
       for (int j = 0; j < KB; ++j) {
-        float kr[DPL];
-        load_row_slice<D>(kc + (kb + j) * D, kr);
+        float2 kr[DP2];
+        load_row_pairs<D>(kc + (kb + j) * D, kr);
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          float a = 0.f;
+          float2 a = __fmul2_rn(q2[g][0], kr[0]);
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) a = fmaf(qv[g][e], kr[e], a);
-          part[j * GP + g] = a;
+          for (int e = 1; e < DP2; ++e) a = ffma2(q2[g][e], kr[e], a);
+          part[j * GP + g] = a.x + a.y;
         }
       }
       reduce_scatter64(part);
@@ -247,7 +268,8 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
 #pragma unroll
         for (int g = 0; g < GP; ++g)
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) acc[g][e] *= alpha[g];
+          for (int e = 0; e < DP2; ++e)
+            acc[g][e] = __fmul2_rn(acc[g][e], make_float2(alpha[g], alpha[g]));
       }
       lpart[0] += p0;
       lpart[1] += p1;
@@ -257,8 +279,8 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
 #pragma unroll
       for (int j = 0; j < KB; ++j) {
         if (kb + j >= n) break;
-        float vr[DPL];
-        load_row_slice<D>(vc + (kb + j) * D, vr);
+        float2 vr[DP2];
+        load_row_pairs<D>(vc + (kb + j) * D, vr);
 #pragma unroll
         for (int g4 = 0; g4 < GP; g4 += 4) {
           const float4 p = *reinterpret_cast<const float4*>(pb + j * GP + g4);
@@ -266,7 +288,8 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[g4 + u][e] = fmaf(pp[u], vr[e], acc[g4 + u][e]);
+            for (int e = 0; e < DP2; ++e)
+              acc[g4 + u][e] = ffma2(make_float2(pp[u], pp[u]), vr[e], acc[g4 + u][e]);
         }
       }
       __syncwarp();
@@ -298,7 +321,8 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
 #pragma unroll
   for (int g = 0; g < GP; ++g)
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) ca[(warp * GP + g) * D + lane * DPL + e] = acc[g][e];
+    for (int e = 0; e < DP2; ++e)
+      *reinterpret_cast<float2*>(ca + (warp * GP + g) * D + lane * DPL + 2 * e) = acc[g][e];
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
   if (sm.abort_flag) return;
   for (int t = threadIdx.x; t < G * D; t += kConsumerWarps * 32) {
@@ -321,8 +345,20 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
 }
 
 // One warp per output row: LSE = log sum_s exp(lse_s); O = sum_s w_s O_s.
-template <typename TO>
-__global__ void __launch_bounds__(256) splitk_merge_kernel(const float* __restrict__ o_part,
+// Lane s computes split s's weight exp(lse_s - LSE) once (32 splits at a time)
+// and the weights are broadcast by shuffles; each lane then accumulates its
+// columns with 16-byte loads when the row allows it.
+__device__ __forceinline__ float merge_max(const float* lp, int nsplit) {
+  const int lane = threadIdx.x & 31;
+  float M = kNegInf;
+  for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, lp[s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  return M;
+}
+
+template <typename TO, bool kVec4>
+__global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            TO* __restrict__ o,
                                                            float* __restrict__ lse, int64_t rows,
@@ -331,22 +367,59 @@ __global__ void __launch_bounds__(256) splitk_merge_kernel(const float* __restri
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const float* lp = lse_part + row * nsplit;
-  float M = kNegInf;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, lp[s]);
+  const float M = merge_max(lp, nsplit);
+  // sum of exp(lse_s - M)
   float tot = 0.f;
   if (M != kNegInf)
-    for (int s = 0; s < nsplit; ++s) tot += expf(lp[s] - M);
+    for (int s = lane; s < nsplit; s += 32) tot += expf(lp[s] - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const float LSE = (M != kNegInf) ? M + logf(tot) : kNegInf;
   const float* op = o_part + row * int64_t(nsplit) * d;
-  for (int c = lane; c < d; c += 32) {
-    float acc = 0.f;
-    if (M != kNegInf)
-      for (int s = 0; s < nsplit; ++s) {
-        const float ls = lp[s];
-        if (ls == kNegInf) continue;
-        acc = fmaf(expf(ls - LSE), op[int64_t(s) * d + c], acc);
+  if constexpr (kVec4) {
+    // lane owns columns [4c, 4c + 4) for c = lane, lane + 32, ...
+    for (int c0 = 0; c0 < d; c0 += 128) {
+      const int c = c0 + 4 * lane;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < nsplit; s0 += 32) {
+        const int s = s0 + lane;
+        const float ls = s < nsplit ? lp[s] : kNegInf;
+        const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
+        const int n = min(32, nsplit - s0);
+        for (int k = 0; k < n; ++k) {
+          const float wk = __shfl_sync(0xffffffffu, w, k);
+          if (c < d && wk != 0.f) {
+            const float4 v = *reinterpret_cast<const float4*>(op + int64_t(s0 + k) * d + c);
+            acc.x = fmaf(wk, v.x, acc.x);
+            acc.y = fmaf(wk, v.y, acc.y);
+            acc.z = fmaf(wk, v.z, acc.z);
+            acc.w = fmaf(wk, v.w, acc.w);
+          }
+        }
       }
-    o[row * d + c] = static_cast<TO>(acc);
+      if (c < d) {
+        o[row * d + c] = static_cast<TO>(acc.x);
+        o[row * d + c + 1] = static_cast<TO>(acc.y);
+        o[row * d + c + 2] = static_cast<TO>(acc.z);
+        o[row * d + c + 3] = static_cast<TO>(acc.w);
+      }
+    }
+  } else {
+    for (int c0 = 0; c0 < d; c0 += 32) {
+      const int c = c0 + lane;
+      float acc = 0.f;
+      for (int s0 = 0; s0 < nsplit; s0 += 32) {
+        const int s = s0 + lane;
+        const float ls = s < nsplit ? lp[s] : kNegInf;
+        const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
+        const int n = min(32, nsplit - s0);
+        for (int k = 0; k < n; ++k) {
+          const float wk = __shfl_sync(0xffffffffu, w, k);
+          if (c < d && wk != 0.f) acc = fmaf(wk, op[int64_t(s0 + k) * d + c], acc);
+        }
+      }
+      if (c < d) o[row * d + c] = static_cast<TO>(acc);
+    }
   }
   if (lane == 0 && lse != nullptr) lse[row] = LSE;
 }
@@ -390,14 +463,24 @@ cudaError_t launch_decode_partials(const void* q, const void* k, const void* v, 
 
 cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                                 int64_t rows, int nsplit, int d, rf_dtype out_dt, cudaStream_t s) {
-  const int warps = 8;
+  const int warps = 4;
   const int64_t grid = (rows + warps - 1) / warps;
-  if (out_dt == RF_F32)
-    splitk_merge_kernel<float><<<static_cast<unsigned>(grid), warps * 32, 0, s>>>(
-        o_part, lse_part, static_cast<float*>(o), lse, rows, nsplit, d);
-  else
-    splitk_merge_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), warps * 32, 0, s>>>(
-        o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, rows, nsplit, d);
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const bool vec = d % 4 == 0 && reinterpret_cast<uintptr_t>(o_part) % 16 == 0;
+  const unsigned g = static_cast<unsigned>(grid);
+  if (out_dt == RF_F32) {
+    float* of = static_cast<float*>(o);
+    if (vec)
+      splitk_merge_kernel<float, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d);
+    else
+      splitk_merge_kernel<float, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d);
+  } else {
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+    if (vec)
+      splitk_merge_kernel<__nv_bfloat16, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d);
+    else
+      splitk_merge_kernel<__nv_bfloat16, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d);
+  }
   return cudaGetLastError();
 }
 
