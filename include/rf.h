@@ -96,10 +96,11 @@ typedef struct {
  * Row softmax: y[r, :] = exp(x[r, :] - max) / sum(exp(x[r, :] - max)).
  * The pure two-reduction cascade of the RedFuser page's problem statement
  * (maximum, then sum of exponentials), single pass over x: a row that fits
- * one CTA (cols <= 32768 for f32) is held on chip between the reductions and
- * the write; longer rows are split over a thread-block cluster that
- * exchanges (max, sum) pairs through distributed shared memory
- * (multi-segment strategy) and, beyond 8 x 32768 columns, re-read once.
+ * one CTA (up to 64 KB: cols <= 16384 for f32) is held on chip between the
+ * reductions and the write; longer rows are split over a cluster of up to 16
+ * CTAs that exchange (max, sum) pairs through distributed shared memory
+ * (multi-segment strategy); rows longer still (or when no such cluster fits)
+ * are read twice.
  *  x, y : [rows, cols] row-major, dtype dt (RF_F32 or RF_BF16); may alias.
  *  rows >= 0, cols >= 0 (either 0: nothing is launched, RF_OK).
  * A row whose entries are all -inf yields zeros. Errors: RF_ERR_INVALID for

@@ -8,16 +8,16 @@
 // (partition, then merge the partial results) strategies.
 //
 // Shapes of the kernel:
-//  * on chip, one CTA per row (row <= kSliceBytes): the row is copied into
+//  * on chip, one CTA per row (row <= 64 KB): the row is copied into
 //    shared memory once (cp.async.bulk, 16 KB pieces, each with its own
 //    mbarrier so the maximum starts on the first piece), then
 //    m = max, p = exp(x - m) written back in place with l = sum p, and
 //    y = p / l stored -- 1 read + 1 write of HBM per element;
-//  * on chip, one cluster of up to 8 CTAs per row (multi-segment): each CTA
+//  * on chip, one cluster of up to 16 CTAs per row (multi-segment): each CTA
 //    reduces its slice to (m_c, l_c), the pairs are exchanged through
 //    distributed shared memory and combined as L = sum_c l_c exp(m_c - M),
 //    and each CTA scales its slice by exp(m_c - M) / L -- still 1R + 1W;
-//  * streaming, one cluster of 8 per row, for rows longer than 8 slices: each
+//  * streaming, one cluster of 8 per row, for rows longer than 16 slices: each
 //    thread folds its elements into a running (m, l) (the incremental form,
 //    O(1) state), the cluster combines, and a second read writes y (2R + 1W).
 // x and y may alias: every element is read before the thread that writes it
@@ -32,10 +32,13 @@ namespace rf {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kSliceBytes = 128 * 1024;  // largest slice one CTA holds on chip
+// Largest slice one CTA holds on chip: 64 KB, so that three CTAs share an SM
+// and one CTA's loads overlap another's stores.
+constexpr int kSliceBytes = 64 * 1024;
 constexpr int kPiece = 16384;            // bytes per bulk copy / mbarrier
 constexpr int kMaxPieces = kSliceBytes / kPiece;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;          // non-portable cluster size (checked at launch)
+constexpr int kStreamCluster = 8;
 
 template <typename T>
 __device__ __forceinline__ float to_f(T v) {
@@ -288,14 +291,22 @@ cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStrea
     const size_t smem = size_t(seg * sizeof(T));
     cudaError_t e = cudaFuncSetAttribute(softmax_rows_onchip<T, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSliceBytes);
+    if (e == cudaSuccess && nc > 8)
+      e = cudaFuncSetAttribute(softmax_rows_onchip<T, true>,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr[0].val.clusterDim.x = nc;
     cfg.gridDim = dim3(static_cast<unsigned>(rows * nc));
     cfg.dynamicSmemBytes = smem;
-    return cudaLaunchKernelEx(&cfg, softmax_rows_onchip<T, true>, x, y, cols, seg,
-                              aligned ? 1 : 0, status);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, softmax_rows_onchip<T, true>, &cfg);
+    if (e == cudaSuccess && clusters > 0)
+      return cudaLaunchKernelEx(&cfg, softmax_rows_onchip<T, true>, x, y, cols, seg,
+                                aligned ? 1 : 0, status);
+    // a cluster this large cannot be placed: fall through to the streaming form
+    (void)cudaGetLastError();
   }
-  const int nc = kMaxCluster;
+  const int nc = kStreamCluster;
   const int64_t seg = (cols + nc - 1) / nc;
   attr[0].val.clusterDim.x = nc;
   cfg.gridDim = dim3(static_cast<unsigned>(rows * nc));
@@ -307,7 +318,7 @@ cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStrea
 
 cudaError_t launch_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols, rf_dtype dt,
                                 cudaStream_t s, int* status) {
-  if (rows * kMaxCluster > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (rows * kMaxCluster > 0x7fffffffLL) return cudaErrorInvalidValue;  // grid size
   if (dt == RF_F32)
     return launch_typed<float>(static_cast<const float*>(x), static_cast<float*>(y), rows, cols,
                                s, status);
