@@ -81,22 +81,43 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
 // exp(x - m) for a finite shift m; exp(-inf - m) = 0.
 __device__ __forceinline__ float exp_shift(float x, float m) { return ex2_approx((x - m) * kLog2e); }
 
+// Cluster barrier halves (barrier.cluster): arrive is non-blocking, wait
+// returns once every CTA of the cluster has arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Combine this CTA's (m, l) with the other CTAs of its cluster through
-// distributed shared memory; every thread gets the row's (M, L).
-__device__ __forceinline__ void cluster_combine(float m, float l, float2* pair, float& M, float& L) {
+// distributed shared memory; every thread gets the row's (M, L). Each CTA
+// pushes its pair into slot [rank] of every peer's `pairs` (one remote store
+// per peer, issued by threads 0..nc-1 at once), then one cluster barrier
+// makes the stores visible and every thread reads its own CTA's array. The
+// caller has arrived (relaxed) on the cluster barrier at kernel start, so the
+// first wait here only confirms that every peer is running before its shared
+// memory is written; no CTA reads a peer's memory after the second barrier,
+// so CTAs may leave as soon as they are done.
+__device__ __forceinline__ void cluster_combine(float m, float l, float2* pairs, float& M,
+                                                float& L) {
   cg::cluster_group cl = cg::this_cluster();
   const unsigned nc = cl.num_blocks();
-  if (threadIdx.x == 0) *pair = make_float2(m, l);
-  cl.sync();
+  cluster_wait_acquire();  // phase 0: every peer has started
+  if (threadIdx.x < nc) *cl.map_shared_rank(pairs + cl.block_rank(), threadIdx.x) = make_float2(m, l);
+  cluster_arrive_release();
+  cluster_wait_acquire();  // phase 1: every pair has landed here
   M = kNegInf;
-  for (unsigned c = 0; c < nc; ++c) M = fmaxf(M, cl.map_shared_rank(pair, c)->x);
+  for (unsigned c = 0; c < nc; ++c) M = fmaxf(M, pairs[c].x);
   L = 0.f;
   if (M != kNegInf)
     for (unsigned c = 0; c < nc; ++c) {
-      const float2 q = *cl.map_shared_rank(pair, c);
+      const float2 q = pairs[c];
       if (q.x != kNegInf) L += q.y * ex2_approx((q.x - M) * kLog2e);
     }
-  cl.sync();  // no CTA leaves while a peer may still read its pair
 }
 
 // Shared-memory-resident slice. The slice [seg0, seg0 + n) of row
@@ -109,10 +130,11 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y
   extern __shared__ __align__(128) unsigned char smem_raw[];
   T* xs = reinterpret_cast<T*>(smem_raw);
   __shared__ float red[32];
-  __shared__ float2 pair;
+  __shared__ float2 pairs[kMaxCluster];
   __shared__ uint64_t bars[kMaxPieces];
   __shared__ int abort_flag;
   const int nc = kCluster ? static_cast<int>(cg::this_cluster().num_blocks()) : 1;
+  if constexpr (kCluster) cluster_arrive_relaxed();  // phase 0 of cluster_combine
   const int64_t row = blockIdx.x / nc;
   const int64_t c = blockIdx.x % nc;
   const int64_t seg0 = c * seg_len;
@@ -170,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y
   float scale;
   if constexpr (kCluster) {
     float M, L;
-    cluster_combine(m, l, &pair, M, L);
+    cluster_combine(m, l, pairs, M, L);
     scale = (L > 0.f && m != kNegInf) ? ex2_approx((m - M) * kLog2e) / L : 0.f;
   } else {
     scale = l > 0.f ? 1.f / l : 0.f;
@@ -221,40 +243,121 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y
   }
 }
 
-// Streaming mode: rows longer than a cluster holds on chip.
+// Unpack one 16-byte vector into floats.
+__device__ __forceinline__ void unpack16(const uint4& w, float (&v)[4]) {
+  v[0] = __uint_as_float(w.x); v[1] = __uint_as_float(w.y);
+  v[2] = __uint_as_float(w.z); v[3] = __uint_as_float(w.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& w, float (&v)[8]) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(in[j] << 16);
+    v[2 * j + 1] = __uint_as_float(in[j] & 0xffff0000u);
+  }
+}
+
+// Fold k values into a running (m, l): one rescale per group, when the
+// group's maximum exceeds m.
+template <int K>
+__device__ __forceinline__ void fold(const float (&v)[K], float& m, float& l) {
+  float vm = v[0];
+#pragma unroll
+  for (int j = 1; j < K; ++j) vm = fmaxf(vm, v[j]);
+  if (vm > m) {
+    l = (m == kNegInf) ? 0.f : l * ex2_approx((m - vm) * kLog2e);
+    m = vm;
+  }
+  if (m != kNegInf) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) l += exp_shift(v[j], m);
+  }
+}
+
+// Streaming mode: rows longer than a cluster holds on chip. With `vec16`
+// the slice is read as 16-byte vectors, four per thread in flight.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y, int64_t cols,
-                                                                int64_t seg_len) {
+                                                                int64_t seg_len, int vec16) {
+  constexpr int V = 16 / sizeof(T);  // elements per vector
+  constexpr int U = 4;               // vectors in flight per thread
   __shared__ float red[32];
-  __shared__ float2 pair;
+  __shared__ float2 pairs[kMaxCluster];
   const int nc = static_cast<int>(cg::this_cluster().num_blocks());
+  cluster_arrive_relaxed();  // phase 0 of cluster_combine
   const int64_t row = blockIdx.x / nc;
   const int64_t c = blockIdx.x % nc;
-  const int64_t seg0 = c * seg_len;
+  const int64_t seg0 = min64(cols, c * seg_len);
   const int64_t seg1 = min64(cols, seg0 + seg_len);
   const T* xr = x + row * cols;
   T* yr = y + row * cols;
   // pass 1: per-thread running (m, l), rescaled whenever m grows
   float m = kNegInf, l = 0.f;
-  for (int64_t e = seg0 + threadIdx.x; e < seg1; e += kThreads) {
-    const float v = to_f(xr[e]);
-    if (v > m) {
-      l = (m == kNegInf) ? 0.f : l * ex2_approx((m - v) * kLog2e);
-      m = v;
+  if (vec16) {  // seg0 and seg1 are multiples of V
+    const uint4* xv = reinterpret_cast<const uint4*>(xr + seg0);
+    const int64_t nv = (seg1 - seg0) / V;
+    for (int64_t b = threadIdx.x; b < nv; b += U * kThreads) {
+      uint4 w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (b + u * kThreads < nv) w[u] = xv[b + u * kThreads];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (b + u * kThreads < nv) {
+          float v[V];
+          unpack16(w[u], v);
+          fold(v, m, l);
+        }
     }
-    if (m != kNegInf) l += exp_shift(v, m);
+  } else {
+    for (int64_t e = seg0 + threadIdx.x; e < seg1; e += kThreads) {
+      const float v[1] = {to_f(xr[e])};
+      fold(v, m, l);
+    }
   }
   // merge the threads' states: block max, then rescaled block sum
   const float bm = block_max(m, red);
   float lt = (m == kNegInf) ? 0.f : l * ex2_approx((m - bm) * kLog2e);
   lt = block_sum(lt, red);
   float M, L;
-  cluster_combine(bm, lt, &pair, M, L);
+  cluster_combine(bm, lt, pairs, M, L);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const float Ms = (M == kNegInf) ? 0.f : M;
   // pass 2: write y
-  for (int64_t e = seg0 + threadIdx.x; e < seg1; e += kThreads)
-    yr[e] = static_cast<T>(exp_shift(to_f(xr[e]), Ms) * inv);
+  if (vec16) {
+    const uint4* xv = reinterpret_cast<const uint4*>(xr + seg0);
+    uint4* yv = reinterpret_cast<uint4*>(yr + seg0);
+    const int64_t nv = (seg1 - seg0) / V;
+    for (int64_t b = threadIdx.x; b < nv; b += U * kThreads) {
+      uint4 w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (b + u * kThreads < nv) w[u] = xv[b + u * kThreads];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (b + u * kThreads < nv) {
+          float v[V];
+          unpack16(w[u], v);
+          uint4 o;
+          if constexpr (V == 4) {
+            o = make_uint4(__float_as_uint(exp_shift(v[0], Ms) * inv),
+                           __float_as_uint(exp_shift(v[1], Ms) * inv),
+                           __float_as_uint(exp_shift(v[2], Ms) * inv),
+                           __float_as_uint(exp_shift(v[3], Ms) * inv));
+          } else {
+            uint32_t p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              p[j] = pack_bf16x2(exp_shift(v[2 * j], Ms) * inv, exp_shift(v[2 * j + 1], Ms) * inv);
+            o = make_uint4(p[0], p[1], p[2], p[3]);
+          }
+          yv[b + u * kThreads] = o;
+        }
+    }
+  } else {
+    for (int64_t e = seg0 + threadIdx.x; e < seg1; e += kThreads)
+      yr[e] = static_cast<T>(exp_shift(to_f(xr[e]), Ms) * inv);
+  }
 }
 
 template <typename T>
@@ -307,11 +410,12 @@ cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStrea
     (void)cudaGetLastError();
   }
   const int nc = kStreamCluster;
-  const int64_t seg = (cols + nc - 1) / nc;
+  int64_t seg = (cols + nc - 1) / nc;
+  seg = (seg + vec - 1) / vec * vec;
   attr[0].val.clusterDim.x = nc;
   cfg.gridDim = dim3(static_cast<unsigned>(rows * nc));
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, softmax_rows_stream<T>, x, y, cols, seg);
+  return cudaLaunchKernelEx(&cfg, softmax_rows_stream<T>, x, y, cols, seg, aligned ? 1 : 0);
 }
 
 }  // namespace

@@ -112,6 +112,24 @@ def test_softmax_rows_edge_values(cuda_device):
     assert_close(xc, y_ref, TOL_F32, "y in place")
 
 
+@pytest.mark.parametrize("cols", [262144, 600000])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_softmax_rows_long_rows_masked_in_place(cuda_device, cols, dtype):
+    """Long rows take the cluster paths (on chip up to 16 slices, streaming
+    beyond): whole slices of -inf, a row with one visible entry and a row with
+    none must combine correctly, in place as well."""
+    x = inputs.make_rows(3, cols, cols + 11, dtype, 3.0)
+    x[0, cols // 3:] = -math.inf          # later CTAs see only -inf
+    x[1, :] = -math.inf                   # nothing visible: zeros
+    x[2, :] = -math.inf
+    x[2, cols - 5] = 0.5                  # one visible entry, in the last slice
+    y_ref = oracle.softmax_rows(f64(x))
+    xc = x.cuda()
+    api.softmax_rows(xc, out=xc)
+    assert api.device_status() == 0
+    assert_close(xc, y_ref, TOL_F32 if dtype == "f32" else TOL_BF16_SOFTMAX, "y in place")
+
+
 def test_blockmask_build_matches_enumeration(cuda_device):
     tm = inputs.random_tile_mask(50, 77, 0.3, 9, nheads=3)
     tm[1, 4, :] = False
