@@ -41,12 +41,22 @@ from online_softmax_attention_rf_gb300 import inputs  # noqa: E402
 WORKLOAD = "mha_prefill"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch from ncu captures (profiles/), valid only for the
+# DRAM traffic per launch from ncu captures (summarised under profiles/), valid only for the
 # kernel source they were taken on; any change to the source makes it null.
 TRAFFIC = {
-    # profiles/attn_tc_mha_prefill.md: dram read 1.996 GB + write 0.125 GB
-    "attn_tc_mha_prefill": {"digest": "9b5c5b0161a2f2a8", "bytes": 2121915904},
+    # attn_tc_kernel<128> on mha_prefill: dram read 403.1 MB + write 111.6 MB
+    "attn_tc_mha_prefill": {"digest": "030bfc2c8de1b9e8", "bytes": 514659328,
+                            "sources": ("attn_tc.cu", "rf_device.cuh")},
+    # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
+    "decode_partials_decode_splitk": {"digest": "bd8db14006de0ee3", "bytes": 4302000000,
+                                      "sources": ("decode.cu", "rf_device.cuh")},
 }
+
+
+def traffic_for(key):
+    """Recorded DRAM bytes per launch, or None once the kernel source changed."""
+    t = TRAFFIC.get(key)
+    return t["bytes"] if t and source_digest(*t["sources"]) == t["digest"] else None
 
 
 def source_digest(*names):
@@ -291,9 +301,7 @@ def run_ours(args, dist, rank, world, local):
 
     att_ms = statistics.mean(per_launch)
     achieved = flops / (att_ms * 1e-3) / 1e12
-    tc_digest = source_digest("attn_tc.cu", "rf_device.cuh")
-    traffic = TRAFFIC.get("attn_tc_mha_prefill")
-    traffic = traffic["bytes"] if traffic and traffic["digest"] == tc_digest else None
+    traffic = traffic_for("attn_tc_mha_prefill")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                 "peak_source": "%s dense bf16 (burst)" % peak_src,
@@ -391,8 +399,10 @@ def bench_decode(args, dev, stream, peaks, peak_src):
            "algorithmic_bytes": algo,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"], "frac_of_8TBs": gbs / 8000.0,
-                        "traffic": None, "peak_source": "%s HBM copy" % peak_src,
-                        "note": "step = partials kernel + merge kernel"}}
+                        "traffic": traffic_for("decode_partials_decode_splitk"),
+                        "peak_source": "%s HBM copy" % peak_src,
+                        "note": "step = partials kernel + merge kernel; traffic is the "
+                                "partials kernel's"}}
     del q, k, v, o, lse, ws
     torch.cuda.empty_cache()
     return out
@@ -424,7 +434,7 @@ def bench_softmax(args, dev, stream, peaks, peak_src):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax"], default="all",
