@@ -16,12 +16,22 @@
 // and a light item of one head so causal work is even across CTAs. Tensor
 // memory, barriers and the pipeline stay live across the items, the second
 // item's Q tiles load as soon as the last QK of the first has read each, and
-// the epilogue of the first overlaps the first MMAs of the second.
-// Warp roles (320 threads):
+// the second item's first QK is issued before the first item's epilogue.
+// Warp roles (352 threads):
 //   warps 0-3  softmax group 0 (query tile 0: thread r owns row r, TMEM lane r)
 //   warps 4-7  softmax group 1 (query tile 1)
-//   warp 8     TMA producer: Q tiles, then K/V tiles into a shared-memory ring
-//   warp 9     TMEM allocator and MMA issuer (one elected lane)
+//   warp 8     TMEM allocator; TMA producer (one lane): Q tiles, then K/V
+//              tiles into a shared-memory ring
+//   warps 9-10 MMA issuers of query tiles 0 and 1 (one lane each)
+// Each query tile has its own issuer. The tensor pipe accepts only a few MMAs
+// ahead of the one executing, so an issuing thread stalls for about as long
+// as its MMAs run; with one issuer per tile the two tiles' MMA streams are
+// independent and one tile's softmax overlaps the other's MMAs. An issuer
+// waits for the K/V tiles of its next block while its softmax group works,
+// because shared-memory waits are slow while the tensor core streams operands
+// from shared memory; it takes P from its group at a named barrier, which is
+// cheap, and pushes each block of MMAs (P.V, then the next Q K^T) under a
+// lock so that the two tiles' blocks reach the pipe whole and in turn.
 // Tensor memory (512 columns): S0 | S1 (128 f32 columns each) | O0 | O1 (D each).
 // P_t (bf16, two per column) is written back into tensor memory and is the A
 // operand of the P.V MMA, so that MMA reads only V from shared memory: at
@@ -35,19 +45,24 @@
 //            if the max grew by more than 2^8, O_t *= a = exp2(m - m') (in TMEM)
 //            else the stale max is kept (a = 1; exact, since l and O share it);
 //            P_t = bf16(p) into tensor memory
-//   MMA:     O_t += P_t V_u
-// The MMA lane issues QK0(u), PV1(u'), QK1(u), PV0(u) (u' the previous key
-// tile), so the softmax of each group overlaps about two MMAs of the other.
+//   MMA:     O_t += P_t V_u, then at once S_t = Q_t K_next^T
 // Epilogue: O = O_t / l (bf16), LSE = (m + log2 l) ln 2.
 //
 // Reuse of S_t's columns for P_t relies on the tensor pipe executing one
 // thread's MMAs in issue order: QK_t(u+1) (which overwrites S_t) is issued after
-// PV_t(u) (which reads P_t from it), as in the published Blackwell attention
-// kernels; the softmax only writes P_t(u+1) after PV_t(u) has completed.
+// PV_t(u) (which reads P_t from it) by the same thread, as in the published
+// Blackwell attention kernels; the commit that signals S_t(u+1) tracks PV_t(u)
+// as well, so the softmax only writes P_t(u+1) after PV_t(u) has completed.
+// A K/V slot is released when both groups are done with it: each group either
+// commits its MMAs that read the slot or, for a key tile only the other group
+// needs, arrives once the tile has landed.
 //
 // Every wait is bounded (RF_WAIT_LIMIT_NS); on expiry the kernel records a
 // status code, the other roles notice the abort flag, and the CTA unwinds,
-// waits for its own copies and MMAs, and frees its tensor memory.
+// waits for its own copies and MMAs, and frees its tensor memory. The five
+// warps of a query tile (its four softmax warps and its issuer) decide to
+// unwind together, at a reducing named barrier, so no warp is ever left
+// waiting at a barrier the others have abandoned.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -63,9 +78,9 @@ namespace {
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 256x
 constexpr int kBM = 128;                   // query rows per tile
 constexpr int kBN = 128;                   // keys per tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpIssue = 9;              // warps 9 and 10: MMA issuers of tiles 0 and 1
 constexpr int kChunk = 16384;              // one 128-row x 64-column bf16 swizzle block
 
 template <int D>
@@ -92,11 +107,11 @@ struct Bars {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
-  uint64_t p_full[2];
   uint64_t o_done[2];
-  uint64_t mma_idle;
+  uint64_t mma_idle[2];
   uint32_t tmem_base;
   int abort_flag;
+  int issue_lock;  // held by a group while it pushes one block of MMAs
 };
 
 // Key-tile list of one query tile: dense/causal range or a block-sparse row.
@@ -167,7 +182,52 @@ struct UnionIter {
     i1 += need1;
     return true;
   }
+  // Whether the next entry exists and is needed by tile t (not consumed).
+  __device__ __forceinline__ bool next_is(int t) const {
+    const int a = i0 < l0.n ? l0.at(i0) : 0x7fffffff;
+    const int b = i1 < l1.n ? l1.at(i1) : 0x7fffffff;
+    if (a == 0x7fffffff && b == 0x7fffffff) return false;
+    return t == 0 ? a <= b : b <= a;
+  }
 };
+
+// Named barrier of one group -- its four softmax warps and its issuer warp,
+// 160 threads, id 1 + t -- that also ORs a predicate over the group: every
+// thread gets the same answer.
+__device__ __forceinline__ bool group_sync_or(int t, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 160, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(1 + t)
+      : "memory");
+  return r != 0;
+}
+
+// The MMA issue lock. An issuer pushes each block of its MMAs (P.V and the
+// next Q K^T) while holding it, so the two tiles' blocks reach the tensor pipe
+// whole and in turn rather than interleaved: the groups then stay half a
+// period apart, each one's softmax running under the other's MMAs. It is
+// taken only after every wait the block needs, so its holder never waits on
+// the other group. Acquisition is bounded like every other wait.
+__device__ __forceinline__ bool issue_lock(int* lk, int* status, int code,
+                                           volatile int* abort_flag) {
+  if (atomicCAS(lk, 0, 1) == 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(32);
+    if (atomicCAS(lk, 0, 1) == 0) return true;
+    if (*abort_flag || globaltimer_ns() - t0 > RF_WAIT_LIMIT_NS) {
+      record_status(status, code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void issue_unlock(int* lk) { atomicExch(lk, 0); }
 
 // Shared-memory descriptors are built once; an MMA step only adds a constant
 // offset (in 16-byte units) to the start-address field, which cannot carry
@@ -234,20 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&bar.kv_full[i], 1);
-      mbar_init(&bar.kv_empty[i], 1);
+      mbar_init(&bar.kv_empty[i], 2);  // one release per softmax group
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar.q_full[t], 1);
       mbar_init(&bar.q_empty[t], 1);
       mbar_init(&bar.s_full[t], 1);
-      mbar_init(&bar.p_full[t], 4);
       mbar_init(&bar.o_done[t], 1);
+      mbar_init(&bar.mma_idle[t], 1);
     }
-    mbar_init(&bar.mma_idle, 1);
     bar.abort_flag = 0;
+    bar.issue_lock = 0;
     fence_barrier_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpLoad) {
     tmem_alloc(&bar.tmem_base, 512);
     tmem_relinquish();
   }
@@ -266,8 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
       int seq = 0;
-      int last[8];
-      for (int i = 0; i < NS; ++i) last[i] = -1;
       int q_loads[2] = {0, 0};
       bool ok = true;
       int bh, qt0;
@@ -289,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < D / 64; ++c)
               tma_load_3d(dst + c * kChunk, kv == 0 ? &tm_k : &tm_v, &bar.kv_full[slot], c * 64,
                           u * kBN, bk);
-            last[slot] = seq;
           }
           if (first && ok) {
             first = false;
@@ -308,138 +365,183 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // never leave with copies in flight
-      for (int i = 0; i < NS; ++i)
-        if (last[i] >= 0)
-          mbar_wait(&bar.kv_full[i], (last[i] / NS) & 1, p.status,
-                    dev_code(kDevTimeout, kKerAttnTc, 11), nullptr);
+      // never leave with copies in flight: the last load into each slot
+      for (int sq = max(0, seq - NS); sq < seq; ++sq)
+        mbar_wait(&bar.kv_full[sq % NS], (sq / NS) & 1, p.status,
+                  dev_code(kDevTimeout, kKerAttnTc, 11), nullptr);
       for (int t = 0; t < 2; ++t)
         if (q_loads[t] > 0)
           mbar_wait(&bar.q_full[t], (q_loads[t] - 1) & 1, p.status,
                     dev_code(kDevTimeout, kKerAttnTc, 13), nullptr);
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    // Issue order per key tile u (previous tile u'):
-    //   QK0(u), PV1(u'), QK1(u), PV0(u)
-    // so each softmax group has about two MMAs of slack between its S being
-    // ready and its P being consumed, and K/V slots are released as early as
-    // their last reader is issued (commit-tracked). After the last QK of a
-    // query tile in an item, its Q buffer is released for the next item.
-    // The tensor pipe buffers only a few MMAs, so this lane keeps the work
-    // between issue blocks minimal: QK_t(u+1) needs no wait of its own,
-    // because it is issued after PV_t(u), which waited for the softmax to have
-    // read S_t(u) and written P_t(u). The commit that signals S_t(u+1) tracks
-    // every earlier MMA of this lane, PV_t(u) included, so the softmax needs
-    // no separate "P.V done" signal except after an item's last P.V.
-    if (lane == 0) {
-      const uint64_t q_desc0 = sdesc_sw128(s_base + L::kOffQ, 16, 1024);
-      const uint64_t q_desc1 = sdesc_sw128(s_base + L::kOffQ + L::kTileBytes, 16, 1024);
-      // K slots are K-major operands, V slots MN-major (64-column blocks
-      // kChunk bytes apart); slot s starts s * kTileBytes after slot 0
-      const uint64_t k_desc0 = sdesc_sw128(s_base + L::kOffKV, 16, 1024);
-      const uint64_t v_desc0 = sdesc_sw128(s_base + L::kOffKV, kChunk, 1024);
-      const uint32_t tm_s0 = tmem + L::kTmemS, tm_s1 = tmem + L::kTmemS + kBN;
-      const uint32_t tm_o0 = tmem + L::kTmemO, tm_o1 = tmem + L::kTmemO + D;
-      const uint32_t tm_p0 = tmem + L::tmem_p(0), tm_p1 = tmem + L::tmem_p(1);
-      int npv0 = 0, npv1 = 0;        // PV tiles issued per query tile (all items)
-      int qu0 = 0, qu1 = 0;          // items whose Q tile has been consumed
-      bool issued_any = false;
-      int seq = 0;
-      bool ok = true;
+  } else if (warp >= kWarpIssue) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp kWarpIssue + t issues and commits the MMAs of query tile t from its
+    // first lane; the other lanes only keep the warp in the group barriers.
+    const int t = warp - kWarpIssue;
+    bool ok = true;
+    // Q_t and the K/V ring as MMA operands: K slots K-major, V slots MN-major
+    // (64-column blocks kChunk bytes apart); slot s starts s * kTileBytes in.
+    const uint64_t q_desc = sdesc_sw128(s_base + L::kOffQ + t * L::kTileBytes, 16, 1024);
+    const uint64_t k_desc0 = sdesc_sw128(s_base + L::kOffKV, 16, 1024);
+    const uint64_t v_desc0 = sdesc_sw128(s_base + L::kOffKV, kChunk, 1024);
+    const uint32_t mm_s = tmem + L::kTmemS + t * kBN;
+    const uint32_t mm_o = tmem + L::kTmemO + t * D;
+    const uint32_t mm_p = tmem + L::tmem_p(t);
+    UnionIter it{};                      // the current item's union of both tiles' lists
+    int seq = 0;                         // K/V sequence number of the next union entry
+    int vseq = 0;                        // V tile of the entry whose QK was issued last
+    int nq = 0;                          // items whose Q_t was waited for
+    int n_iss = 0;                       // entries of this item issued (QK) so far
+    int started = -1;                    // last item whose first QK was issued
+    bool issued_any = false;
+    int ibh = 0, iqt0 = 0;               // item the issuer is on
 #define RF_WAIT(b, par, site)                                                        \
   mbar_wait(&bar.b, (par), p.status, dev_code(kDevTimeout, kKerAttnTc, site), abort_flag)
 #define RF_SLOT(sq) (static_cast<uint64_t>((((sq) % NS) * L::kTileBytes) >> 4))
-      int bh, qt0;
-      for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
-        UnionIter it{tile_list(p, bh, qt0, true), tile_list(p, bh, qt0 + 1, true)};
-        bool qr0 = false, qr1 = false;   // Q tile present for this item
-        bool acc0 = false, acc1 = false; // O_t holds this item's partial sum
-        int pend1 = -1;                  // V load sequence number tile 1 still owes
-        bool pend1_v_ready = false;
-        int u;
-        bool need0, need1;
-        while (it.next(u, need0, need1)) {
-          const int kseq = seq, vseq = seq + 1;
-          seq += 2;
-          if (!(ok = RF_WAIT(kv_full[kseq % NS], (kseq / NS) & 1, 21))) break;
-          const uint64_t kd = k_desc0 + RF_SLOT(kseq);
-          if (need0) {
-            if (!qr0) {
-              if (!(ok = RF_WAIT(q_full[0], qu0 & 1, 22))) break;
-              qr0 = true;
-            }
-            issue_qk<D>(tm_s0, q_desc0, kd);
-            mma_commit(&bar.s_full[0]);
-            issued_any = true;
-            if (it.i0 == it.l0.n) {  // last QK on Q0 in this item
-              mma_commit(&bar.q_empty[0]);
-              ++qu0;
-            }
-            if (p.visited != nullptr) p.visited[(int64_t(bh) * p.nqt + qt0) * p.nkt + u] = 1;
-          }
-          if (pend1 >= 0) {
-            if (!pend1_v_ready && !(ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 24))) break;
-            if (!(ok = RF_WAIT(p_full[1], npv1 & 1, 25))) break;
-            tc_fence_after_sync();
-            issue_pv<D>(tm_o1, tm_p1, v_desc0 + RF_SLOT(pend1), acc1);
-            acc1 = true;
-            ++npv1;
-            if (!need1 && it.i1 == it.l1.n) mma_commit(&bar.o_done[1]);  // item's last on O1
-            mma_commit(&bar.kv_empty[pend1 % NS]);
-            pend1 = -1;
-          }
-          if (need1) {
-            if (!qr1) {
-              if (!(ok = RF_WAIT(q_full[1], qu1 & 1, 22))) break;
-              qr1 = true;
-            }
-            issue_qk<D>(tm_s1, q_desc1, kd);
-            mma_commit(&bar.s_full[1]);
-            issued_any = true;
-            if (it.i1 == it.l1.n) {
-              mma_commit(&bar.q_empty[1]);
-              ++qu1;
-            }
-            if (p.visited != nullptr)
-              p.visited[(int64_t(bh) * p.nqt + qt0 + 1) * p.nkt + u] = 1;
-          }
-          mma_commit(&bar.kv_empty[kseq % NS]);
-          if (need0) {
-            if (!(ok = RF_WAIT(kv_full[vseq % NS], (vseq / NS) & 1, 24))) break;
-            if (!(ok = RF_WAIT(p_full[0], npv0 & 1, 25))) break;
-            tc_fence_after_sync();
-            issue_pv<D>(tm_o0, tm_p0, v_desc0 + RF_SLOT(vseq), acc0);
-            acc0 = true;
-            ++npv0;
-            if (it.i0 == it.l0.n) mma_commit(&bar.o_done[0]);  // item's last P.V on O0
-          }
-          if (need1) {
-            pend1 = vseq;
-            pend1_v_ready = need0;  // PV0 has already waited for this V tile
-          } else {
-            mma_commit(&bar.kv_empty[vseq % NS]);
-          }
+    // Next union entry this group needs; entries only the other group needs
+    // are released (both slots) once they have landed. False at the item's end.
+    auto advance = [&](int& u, int& kseq) -> bool {
+      int uu;
+      bool n0, n1;
+      while (it.next(uu, n0, n1)) {
+        const int ks = seq;
+        seq += 2;
+        if (t == 0 ? n0 : n1) {
+          u = uu;
+          kseq = ks;
+          return true;
         }
-        if (ok && pend1 >= 0) {
-          if ((pend1_v_ready || (ok = RF_WAIT(kv_full[pend1 % NS], (pend1 / NS) & 1, 26))) &&
-              (ok = RF_WAIT(p_full[1], npv1 & 1, 27))) {
-            tc_fence_after_sync();
-            issue_pv<D>(tm_o1, tm_p1, v_desc0 + RF_SLOT(pend1), acc1);
-            ++npv1;
-            mma_commit(&bar.o_done[1]);
-            mma_commit(&bar.kv_empty[pend1 % NS]);
-          }
+        for (int e = 0; e < 2; ++e) {
+          if (!(ok = RF_WAIT(kv_full[(ks + e) % NS], ((ks + e) / NS) & 1, 20))) return false;
+          mbar_arrive(&bar.kv_empty[(ks + e) % NS]);
         }
       }
+      return false;
+    };
+#define RF_LOCK() issue_lock(&bar.issue_lock, p.status, dev_code(kDevTimeout, kKerAttnTc, 23), abort_flag)
+    // The next entry this group needs, with its K tile landed; false at the
+    // item's end or on failure (ok).
+    auto next_k = [&](int& u, int& kseq) -> bool {
+      if (!advance(u, kseq)) return false;
+      return (ok = RF_WAIT(kv_full[kseq % NS], (kseq / NS) & 1, 21));
+    };
+    // Commits after S_t = Q_t K_u^T (K in slot kseq) has been issued, the
+    // one the softmax waits for first; they track every earlier MMA of this
+    // thread, so they need not hold the lock.
+    auto qk_commits = [&](int u, int kseq, int n) {
+      mma_commit(&bar.s_full[t]);
+      mma_commit(&bar.kv_empty[kseq % NS]);
+      if (++n_iss == n) mma_commit(&bar.q_empty[t]);  // the item's last read of Q_t
+      vseq = kseq + 1;
+      if (p.visited != nullptr)
+        p.visited[(int64_t(ibh) * p.nqt + iqt0 + t) * p.nkt + u] = 1;
+    };
+    // Item k: wait for its Q_t and issue its first QK (or, when this group
+    // has no key tile in it, release all of its entries).
+    auto start_item = [&](int k) {
+      started = k;
+      if (!cta_item(p, k, ibh, iqt0)) return;
+      it = UnionIter{tile_list(p, ibh, iqt0, t == 0), tile_list(p, ibh, iqt0 + 1, t == 1)};
+      n_iss = 0;
+      const int n = t == 0 ? it.l0.n : it.l1.n;
+      if (n == 0) {
+        int u, kseq;
+        advance(u, kseq);  // releases every entry; returns false
+        return;
+      }
+      if (!(ok = RF_WAIT(q_full[t], nq & 1, 22))) return;
+      ++nq;
+      int u, kseq;
+      if (next_k(u, kseq) && (ok = RF_LOCK())) {
+        tc_fence_after_sync();
+        issue_qk<D>(mm_s, q_desc, k_desc0 + RF_SLOT(kseq));
+        issue_unlock(&bar.issue_lock);
+        issued_any = true;
+        qk_commits(u, kseq, n);
+      }
+    };
+
+    // The same items, lists and group barriers as the softmax warps.
+    int bh, qt0;
+    for (int item = 0; cta_item(p, item, bh, qt0); ++item) {
+      const TileList list = tile_list(p, bh, qt0 + t, false);
+      if (lane == 0 && started < item) start_item(item);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      for (int jj = 0; jj < list.n; ++jj) {
+        // Prepare this step's MMA block while the softmax runs: wait for V_u
+        // and, when the next union entry is this group's, for that entry's K
+        // tile, and consume the entry. Blocking on that K tile before this
+        // step's P.V is safe: with no skipped entry between, its slot was
+        // freed by releases committed in earlier blocks.
+        const bool last = jj + 1 == list.n;
+        int u2 = 0, k2 = 0;
+        bool fast = false;
+        if (lane == 0 && ok && (ok = RF_WAIT(kv_full[vseq % NS], (vseq / NS) & 1, 24)) && !last &&
+            it.next_is(t) && (ok = RF_WAIT(kv_full[seq % NS], (seq / NS) & 1, 21))) {
+          advance(u2, k2);  // consumes exactly that entry
+          fast = true;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        // P_t is in tensor memory
+        if (group_sync_or(t, !ok)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0 && (ok = RF_LOCK())) {
+          // O_t += P_t V_u, then the next QK of this group in the same block
+          // when it was prepared above, or the end of the item. Only the MMAs
+          // are issued under the lock; the commits follow it, S first. P.V is
+          // issued before any wait that may block: the next K tile, or a tile
+          // this group skips, may be loaded only into the slot this P.V
+          // releases.
+          tc_fence_after_sync();
+          issue_pv<D>(mm_o, mm_p, v_desc0 + RF_SLOT(vseq), jj > 0);
+          if (fast) issue_qk<D>(mm_s, q_desc, k_desc0 + RF_SLOT(k2));
+          issue_unlock(&bar.issue_lock);
+          const int v_done = vseq;
+          if (fast) {
+            qk_commits(u2, k2, list.n);
+            mma_commit(&bar.kv_empty[v_done % NS]);
+          } else {
+            mma_commit(&bar.kv_empty[v_done % NS]);
+            if (last) {
+              mma_commit(&bar.o_done[t]);
+            } else if (next_k(u2, k2) && (ok = RF_LOCK())) {
+              tc_fence_after_sync();
+              issue_qk<D>(mm_s, q_desc, k_desc0 + RF_SLOT(k2));
+              issue_unlock(&bar.issue_lock);
+              qk_commits(u2, k2, list.n);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      if (group_sync_or(t, !ok)) {  // after the item's steps
+        ok = false;
+        break;
+      }
+      // while the softmax warps write this item's output: release the
+      // entries after this group's last, and start the next item
+      if (lane == 0 && list.n > 0) {
+        int u2, k2;
+        advance(u2, k2);
+        if (ok) start_item(item + 1);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (group_sync_or(t, !ok)) {  // after the item's epilogue
+        ok = false;
+        break;
+      }
+    }
 #undef RF_WAIT
 #undef RF_SLOT
-      // never leave with MMAs in flight (their operands live in this CTA)
-      if (issued_any) {
-        mma_commit(&bar.mma_idle);
-        mbar_wait(&bar.mma_idle, 0, p.status, dev_code(kDevTimeout, kKerAttnTc, 28), nullptr);
-      }
+#undef RF_LOCK
+    // never leave with MMAs in flight (their operands live in this CTA)
+    if (lane == 0 && issued_any) {
+      mma_commit(&bar.mma_idle[t]);
+      mbar_wait(&bar.mma_idle[t], 0, p.status, dev_code(kDevTimeout, kKerAttnTc, 28), nullptr);
     }
     __syncwarp();
   } else {
@@ -454,8 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int j = 0;                           // S tiles consumed (all items)
     int o_items = 0;                     // items whose final P.V was waited for
     bool ok = true;
+    // Every exit from the loops below is decided at a group barrier that the
+    // group's issuer warp joins too, so the five warps always leave together.
     int bh, qt0;
-    for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
+    for (int item = 0; cta_item(p, item, bh, qt0); ++item) {
       const int qt = qt0 + t;
       const int64_t row = int64_t(qt) * kBM + r;
       const TileList list = tile_list(p, bh, qt, false);
@@ -463,97 +567,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t tile_first_lim =
           p.causal ? min64(p.Sk, int64_t(qt) * kBM + 1 + shift) : p.Sk;
       float m_run = kNegInf, l_run = 0.f;
-      for (int jj = 0; jj < list.n && ok; ++jj, ++j) {
+      for (int jj = 0; jj < list.n; ++jj, ++j) {
         const int u = list.at(jj);
-        ok = mbar_wait_warp(&bar.s_full[t], j & 1, p.status,
-                            dev_code(kDevTimeout, kKerAttnTc, 30), abort_flag);
-        if (!ok) break;
-        tc_fence_after_sync();
-        // element mask only where the tile crosses the causal diagonal or Sk
-        const int64_t k0 = int64_t(u) * kBN;
-        const int lim = (k0 + kBN > tile_first_lim)
-                            ? static_cast<int>(max64(int64_t(0), min64(kBN, row_lim - k0)))
-                            : kBN;
-        // pass 1: row maximum over all 128 columns (one TMEM read), 8
-        // independent partial maxima, two columns per step (max is exact, so
-        // the order does not matter)
-        float mx;
-        {
-          uint32_t sr[128];
-          tmem_ld128_wait(tm_s, sr);
-          if (lim < kBN) {
+        if (ok)
+          ok = mbar_wait_warp(&bar.s_full[t], j & 1, p.status,
+                              dev_code(kDevTimeout, kKerAttnTc, 30), abort_flag);
+        if (ok) {
+          tc_fence_after_sync();
+          // element mask only where the tile crosses the causal diagonal or Sk
+          const int64_t k0 = int64_t(u) * kBN;
+          const int lim = (k0 + kBN > tile_first_lim)
+                              ? static_cast<int>(max64(int64_t(0), min64(kBN, row_lim - k0)))
+                              : kBN;
+          // pass 1: row maximum over the 128 columns, read from tensor memory
+          // in two halves of 64 (registers stay below the cap), 8 independent
+          // partial maxima, two columns per step (max is exact, so the order
+          // does not matter)
+          float mx;
+          {
+            float m8[8];
 #pragma unroll
-            for (int c = 0; c < kBN; ++c)
-              if (c >= lim) sr[c] = __float_as_uint(kNegInf);
-          }
-          float m8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = kNegInf;
-#pragma unroll
-          for (int c = 0; c < kBN; c += 2)
-            m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sr[c]),
-                                     __uint_as_float(sr[c + 1]));
-          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                     fmaxf(m8[6], m8[7]));
-        }
-        const float m_new = (mx == kNegInf) ? m_run : fmaxf(m_run, mx * p.scale_log2);
-        const bool resc = m_new > m_run + kRescaleThreshold;
-        const float m_use = resc ? m_new : m_run;
-        const float alpha = resc ? ex2_approx(m_run - m_new) : 1.f;
-        const float sh = (m_use == kNegInf) ? 0.f : m_use;
-        // (the previous P.V on O_t and P_t has completed: the commit that
-        // signalled this S tracks it)
-        // pass 2: p = exp2(s * c - m) two columns at a time (packed FMA), row
-        // sum in 4 packed partial sums, P as bf16 pairs (column j = keys 2j,
-        // 2j+1). Half h reads S columns [64h, 64h + 64) and writes P columns
-        // [32h, 32h + 32); at D = 128 P sits on S's first 64 columns, which
-        // half 0 has already read.
-        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-        const float2 nsh2 = make_float2(-sh, -sh);
-        float2 s4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s4[i] = make_float2(0.f, 0.f);
+            for (int i = 0; i < 8; ++i) m8[i] = kNegInf;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sr[64];
-          tmem_ld64_wait(tm_s + 64 * h, sr);
-          if (lim < kBN) {
+            for (int h = 0; h < 2; ++h) {
+              uint32_t sr[64];
+              tmem_ld64_wait(tm_s + 64 * h, sr);
+              if (lim < kBN) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (64 * h + c >= lim) sr[c] = __float_as_uint(kNegInf);
-          }
-          uint32_t pw[32];
+                for (int c = 0; c < 64; ++c)
+                  if (64 * h + c >= lim) sr[c] = __float_as_uint(kNegInf);
+              }
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float2 x = ffma2(
-                make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nsh2);
-            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            s4[(c >> 1) & 3] = fadd2(s4[(c >> 1) & 3], pp);
-            pw[c >> 1] = pack_bf16x2(pp.x, pp.y);
+              for (int c = 0; c < 64; c += 2)
+                m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sr[c]),
+                                         __uint_as_float(sr[c + 1]));
+            }
+            mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                       fmaxf(m8[6], m8[7]));
           }
-          tmem_st32(tm_p + 32 * h, pw);
-        }
-        tmem_wait_st();
-        const float2 st = fadd2(fadd2(s4[0], s4[1]), fadd2(s4[2], s4[3]));
-        l_run = l_run * alpha + (st.x + st.y);
-        m_run = m_use;
-        if (jj > 0 && __any_sync(0xffffffffu, resc)) {
+          const float m_new = (mx == kNegInf) ? m_run : fmaxf(m_run, mx * p.scale_log2);
+          const bool resc = m_new > m_run + kRescaleThreshold;
+          const float m_use = resc ? m_new : m_run;
+          const float alpha = resc ? ex2_approx(m_run - m_new) : 1.f;
+          const float sh = (m_use == kNegInf) ? 0.f : m_use;
+          // pass 2: p = exp2(s * c - m) two columns at a time (packed FMA),
+          // row sum in 4 packed partial sums, P as bf16 pairs (column j =
+          // keys 2j, 2j+1). Half h reads S columns [64h, 64h + 64) and writes
+          // P columns [32h, 32h + 32); at D = 128 P sits on S's first 64
+          // columns, which half 0 has already read.
+          const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+          const float2 nsh2 = make_float2(-sh, -sh);
+          float2 s4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s4[i] = make_float2(0.f, 0.f);
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t ov[32];
-            tmem_ld32_wait(tm_o + c, ov);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t sr[64];
+            tmem_ld64_wait(tm_s + 64 * h, sr);
+            if (lim < kBN) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32_wait(tm_o + c, ov);
+              for (int c = 0; c < 64; ++c)
+                if (64 * h + c >= lim) sr[c] = __float_as_uint(kNegInf);
+            }
+            uint32_t pw[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+              const float2 x = ffma2(
+                  make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nsh2);
+              const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              s4[(c >> 1) & 3] = fadd2(s4[(c >> 1) & 3], pp);
+              pw[c >> 1] = pack_bf16x2(pp.x, pp.y);
+            }
+            tmem_st32(tm_p + 32 * h, pw);
           }
+          tmem_wait_st();
+          const float2 st = fadd2(fadd2(s4[0], s4[1]), fadd2(s4[2], s4[3]));
+          l_run = l_run * alpha + (st.x + st.y);
+          m_run = m_use;
+          // O_t *= alpha; the previous P.V on O_t has completed (the commit
+          // that signalled this S tracks it)
+          if (jj > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t ov[32];
+              tmem_ld32_wait(tm_o + c, ov);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tmem_st32_wait(tm_o + c, ov);
+            }
+          }
+          tc_fence_before_sync();
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.p_full[t]);
+        // P_t (and any rescale of O_t) is in tensor memory for all 128 rows;
+        // the group's issuer warp takes it from here
+        if (group_sync_or(t, !ok)) {
+          ok = false;
+          break;
+        }
       }
-      if (!ok) break;
+      // the issuer has committed the item's last P.V (or given up)
+      if (group_sync_or(t, !ok)) {
+        ok = false;
+        break;
+      }
       // epilogue: O = acc / l, LSE = (m + log2 l) ln 2. The next item's first
-      // P.V on O_t is issued only after this group's next P arrives, i.e.
+      // P.V on O_t is issued only after this group's next P is written, i.e.
       // after the TMEM reads below.
       const bool row_ok = row < p.Sq && qt < p.nqt;
       __nv_bfloat16* og = p.o + (int64_t(bh) * p.Sq + row) * D;
@@ -561,7 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_warp(&bar.o_done[t], o_items & 1, p.status,
                             dev_code(kDevTimeout, kKerAttnTc, 32), abort_flag);
         ++o_items;
-        if (!ok) break;
+      }
+      if (list.n > 0 && ok) {
         tc_fence_after_sync();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
@@ -583,10 +703,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before_sync();
         if (row_ok && p.lse != nullptr)
           p.lse[int64_t(bh) * p.Sq + row] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : kNegInf;
-      } else if (row_ok) {
+      } else if (list.n == 0 && row_ok) {
         // no visible key for any row of this tile
         for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(og + c) = make_uint4(0, 0, 0, 0);
         if (p.lse != nullptr) p.lse[int64_t(bh) * p.Sq + row] = kNegInf;
+      }
+      if (group_sync_or(t, !ok)) {
+        ok = false;
+        break;
       }
     }
   }
@@ -594,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpLoad) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
