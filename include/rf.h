@@ -119,7 +119,8 @@ rf_status rf_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
  * tiles, tcgen05 MMAs into tensor memory); RF_F32 with d % 4 == 0 and
  * d <= 256 (exact SIMT kernel, one warp per query row).
  * Pointers must be 16-byte aligned. B, H, Hkv >= 1; H % Hkv == 0;
- * Sq, Sk >= 0 (Sq == 0: nothing launched; Sk == 0: O = 0, lse = -inf).
+ * 0 <= Sq, Sk <= 2^30 (Sq == 0: nothing launched; Sk == 0: O = 0,
+ * lse = -inf).
  * Errors: RF_ERR_INVALID (NULL/misaligned pointers, bad sizes, H % Hkv,
  * scale <= 0, blockmask fields inconsistent with Sq/Sk); RF_ERR_UNSUPPORTED
  * (dtype/d combination not listed above).

@@ -127,6 +127,8 @@ rf_status rf_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
   if (B < 1 || H < 1 || Hkv < 1 || Sq < 0 || Sk < 0 || d < 1)
     return fail(RF_ERR_INVALID, "rf_attn_fwd: bad sizes B=%d H=%d Hkv=%d Sq=%d Sk=%d d=%d", B, H,
                 Hkv, Sq, Sk, d);
+  if (Sq > (1 << 30) || Sk > (1 << 30))
+    return fail(RF_ERR_INVALID, "rf_attn_fwd: Sq and Sk must be <= 2^30");
   if (H % Hkv != 0) return fail(RF_ERR_INVALID, "rf_attn_fwd: H %% Hkv != 0");
   if (!(scale > 0.f) || !std::isfinite(scale))
     return fail(RF_ERR_INVALID, "rf_attn_fwd: scale must be finite and > 0");
