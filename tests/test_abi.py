@@ -68,6 +68,8 @@ def _attn(L, q=A, k=A, v=A, o=A, lse=A, B=1, H=4, Hkv=2, Sq=256, Sk=256, d=128, 
     (dict(causal=2), api.RF_ERR_INVALID),
     (dict(B=0), api.RF_ERR_INVALID),
     (dict(Sq=-1), api.RF_ERR_INVALID),
+    (dict(Sq=(1 << 30) + 1), api.RF_ERR_INVALID),       # row indices stay 32-bit
+    (dict(Sk=(1 << 30) + 1), api.RF_ERR_INVALID),
     (dict(d=96), api.RF_ERR_UNSUPPORTED),            # bf16 head dims: 64, 128
     (dict(d=258, dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
     (dict(d=66, dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
