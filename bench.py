@@ -44,8 +44,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch from ncu captures (summarised under profiles/), valid only for the
 # kernel source they were taken on; any change to the source makes it null.
 TRAFFIC = {
-    # attn_tc_kernel<128> on mha_prefill: dram read 403.1 MB + write 111.6 MB
-    "attn_tc_mha_prefill": {"digest": "030bfc2c8de1b9e8", "bytes": 514659328,
+    # attn_tc_kernel<128> on mha_prefill: dram read 404.1 MB + write 113.4 MB
+    "attn_tc_mha_prefill": {"digest": "8e3f74714654c23b", "bytes": 517469184,
                             "sources": ("attn_tc.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
     "decode_partials_decode_splitk": {"digest": "bd8db14006de0ee3", "bytes": 4302000000,
