@@ -95,12 +95,13 @@ typedef struct {
 /*
  * Row softmax: y[r, :] = exp(x[r, :] - max) / sum(exp(x[r, :] - max)).
  * The pure two-reduction cascade of the RedFuser page's problem statement
- * (maximum, then sum of exponentials), single pass over x: a row that fits
- * one CTA (up to 64 KB: cols <= 16384 for f32) is held on chip between the
- * reductions and the write; longer rows are split over a cluster of up to 16
- * CTAs that exchange (max, sum) pairs through distributed shared memory
- * (multi-segment strategy); rows longer still (or when no such cluster fits)
- * are read twice.
+ * (maximum, then sum of exponentials), one read and one write of x per
+ * element in HBM: a row that fits one CTA (up to 64 KB: cols <= 16384 for
+ * f32) is held in shared memory between the reductions and the write; a
+ * longer row is split over a cluster of 2..16 CTAs (about 64 KB each) that
+ * exchange (max, sum) pairs through distributed shared memory (multi-segment
+ * strategy) and read their slice a second time from L2, where the first
+ * read left it.
  *  x, y : [rows, cols] row-major, dtype dt (RF_F32 or RF_BF16); may alias.
  *  rows >= 0, cols >= 0 (either 0: nothing is launched, RF_OK).
  * A row whose entries are all -inf yields zeros. Errors: RF_ERR_INVALID for

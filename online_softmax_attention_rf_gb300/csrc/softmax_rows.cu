@@ -13,13 +13,17 @@
 //    mbarrier so the maximum starts on the first piece), then
 //    m = max, p = exp(x - m) written back in place with l = sum p, and
 //    y = p / l stored -- 1 read + 1 write of HBM per element;
-//  * on chip, one cluster of up to 16 CTAs per row (multi-segment): each CTA
-//    reduces its slice to (m_c, l_c), the pairs are exchanged through
-//    distributed shared memory and combined as L = sum_c l_c exp(m_c - M),
-//    and each CTA scales its slice by exp(m_c - M) / L -- still 1R + 1W;
-//  * streaming, one cluster of 8 per row, for rows longer than 16 slices: each
-//    thread folds its elements into a running (m, l) (the incremental form,
-//    O(1) state), the cluster combines, and a second read writes y (2R + 1W).
+//  * longer rows, one cluster of 2..16 CTAs per row (multi-segment), about
+//    64 KB of the row per CTA: each thread folds its elements into a running
+//    (m, l) (the incremental form, O(1) state), the CTAs exchange their
+//    (m_c, l_c) through distributed shared memory and combine them as
+//    L = sum_c l_c exp(m_c - M), and a second pass over the slice writes y.
+//    The first pass loads with an L2 evict-last policy and the second with
+//    evict-first, so the slice is re-read from the 126 MB L2 rather than HBM
+//    (a grid's slices in flight, ~40 MB, fit in it): HBM still sees 1 read +
+//    1 write per element. (Keeping the slice in shared memory instead, with
+//    the whole cluster waiting for its slowest CTA before any CTA can store,
+//    measured 30 % slower.)
 // x and y may alias: every element is read before the thread that writes it
 // writes it.
 #include <cooperative_groups.h>
@@ -33,12 +37,12 @@ namespace {
 
 constexpr int kThreads = 512;
 // Largest slice one CTA holds on chip: 64 KB, so that three CTAs share an SM
-// and one CTA's loads overlap another's stores.
+// and one CTA's loads overlap another's stores. Long rows give each CTA of a
+// cluster about as much.
 constexpr int kSliceBytes = 64 * 1024;
 constexpr int kPiece = 16384;            // bytes per bulk copy / mbarrier
 constexpr int kMaxPieces = kSliceBytes / kPiece;
 constexpr int kMaxCluster = 16;          // non-portable cluster size (checked at launch)
-constexpr int kStreamCluster = 8;
 
 template <typename T>
 __device__ __forceinline__ float to_f(T v) {
@@ -120,27 +124,21 @@ __device__ __forceinline__ void cluster_combine(float m, float l, float2* pairs,
     }
 }
 
-// Shared-memory-resident slice. The slice [seg0, seg0 + n) of row
-// blockIdx / nc is staged in dynamic shared memory as T; float input keeps
-// the probabilities in place, bf16 input keeps x and recomputes the exp.
-template <typename T, bool kCluster>
+// Shared-memory-resident row. Row blockIdx is staged in dynamic shared
+// memory as T; float input keeps the probabilities in place, bf16 input keeps
+// x and recomputes the exp.
+template <typename T>
 __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y, int64_t cols,
-                                                                int64_t seg_len, int bulk,
-                                                                int* status) {
+                                                                int bulk, int* status) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   T* xs = reinterpret_cast<T*>(smem_raw);
   __shared__ float red[32];
-  __shared__ float2 pairs[kMaxCluster];
   __shared__ uint64_t bars[kMaxPieces];
   __shared__ int abort_flag;
-  const int nc = kCluster ? static_cast<int>(cg::this_cluster().num_blocks()) : 1;
-  if constexpr (kCluster) cluster_arrive_relaxed();  // phase 0 of cluster_combine
-  const int64_t row = blockIdx.x / nc;
-  const int64_t c = blockIdx.x % nc;
-  const int64_t seg0 = c * seg_len;
-  const int64_t n = min64(cols, seg0 + seg_len) - seg0;  // may be <= 0 for a last CTA
-  const T* xr = x + row * cols + seg0;
-  T* yr = y + row * cols + seg0;
+  const int64_t row = blockIdx.x;
+  const int64_t n = cols;
+  const T* xr = x + row * cols;
+  T* yr = y + row * cols;
   constexpr int kPerPiece = kPiece / sizeof(T);
   const int npieces = n > 0 ? static_cast<int>((n + kPerPiece - 1) / kPerPiece) : 0;
 
@@ -189,14 +187,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y
     }
   }
   l = block_sum(l, red);
-  float scale;
-  if constexpr (kCluster) {
-    float M, L;
-    cluster_combine(m, l, pairs, M, L);
-    scale = (L > 0.f && m != kNegInf) ? ex2_approx((m - M) * kLog2e) / L : 0.f;
-  } else {
-    scale = l > 0.f ? 1.f / l : 0.f;
-  }
+  const float scale = l > 0.f ? 1.f / l : 0.f;
   if (abort_flag) {  // uniform: set before the last block reduction
     // never leave with copies in flight
     if (bulk && threadIdx.x == 0)
@@ -274,13 +265,16 @@ __device__ __forceinline__ void fold(const float (&v)[K], float& m, float& l) {
   }
 }
 
-// Streaming mode: rows longer than a cluster holds on chip. With `vec16`
-// the slice is read as 16-byte vectors, four per thread in flight.
+// Long rows, one cluster per row, slice [seg0, seg1) per CTA. With `vec16`
+// the slice is read as 16-byte vectors, four per thread in flight, pass 1
+// with an L2 evict-last policy so that pass 2 (evict-first, like the stores
+// of y) finds it in L2.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y, int64_t cols,
                                                                 int64_t seg_len, int vec16) {
   constexpr int V = 16 / sizeof(T);  // elements per vector
   constexpr int U = 4;               // vectors in flight per thread
+  const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
   __shared__ float red[32];
   __shared__ float2 pairs[kMaxCluster];
   const int nc = static_cast<int>(cg::this_cluster().num_blocks());
@@ -300,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y
       uint4 w[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (b + u * kThreads < nv) w[u] = xv[b + u * kThreads];
+        if (b + u * kThreads < nv) w[u] = ld_global_policy(xv + b + u * kThreads, keep);
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (b + u * kThreads < nv) {
@@ -332,7 +326,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y
       uint4 w[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (b + u * kThreads < nv) w[u] = xv[b + u * kThreads];
+        if (b + u * kThreads < nv) w[u] = ld_global_policy(xv + b + u * kThreads, drop);
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (b + u * kThreads < nv) {
@@ -351,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y
               p[j] = pack_bf16x2(exp_shift(v[2 * j], Ms) * inv, exp_shift(v[2 * j + 1], Ms) * inv);
             o = make_uint4(p[0], p[1], p[2], p[3]);
           }
-          yv[b + u * kThreads] = o;
+          st_global_policy(yv + b + u * kThreads, o, drop);
         }
     }
   } else {
@@ -363,20 +357,22 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y
 template <typename T>
 cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStream_t s,
                          int* status) {
-  constexpr int64_t cap = kSliceBytes / sizeof(T);  // elements per CTA on chip
+  constexpr int64_t cap = kSliceBytes / sizeof(T);  // elements per CTA
   constexpr int64_t vec = 16 / sizeof(T);
-  // bulk copies need 16-byte aligned slices of whole 16-byte vectors
+  // bulk copies and vector loads need 16-byte aligned rows of whole vectors
   const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                        (reinterpret_cast<uintptr_t>(y) % 16 == 0) && cols % vec == 0;
   if (cols <= cap) {
     const size_t smem = size_t((cols * sizeof(T) + 15) / 16 * 16);
-    cudaError_t e = cudaFuncSetAttribute(softmax_rows_onchip<T, false>,
+    cudaError_t e = cudaFuncSetAttribute(softmax_rows_onchip<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSliceBytes);
     if (e != cudaSuccess) return e;
-    softmax_rows_onchip<T, false><<<static_cast<unsigned>(rows), kThreads, smem, s>>>(
-        x, y, cols, cols, aligned ? 1 : 0, status);
+    softmax_rows_onchip<T><<<static_cast<unsigned>(rows), kThreads, smem, s>>>(
+        x, y, cols, aligned ? 1 : 0, status);
     return cudaGetLastError();
   }
+  // one cluster per row, about one slice per CTA
+  int nc = static_cast<int>(min64(kMaxCluster, max64(2, (cols + cap - 1) / cap)));
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -386,35 +382,24 @@ cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStrea
   cfg.numAttrs = 1;
   cfg.stream = s;
   cfg.blockDim = dim3(kThreads);
-  if (cols <= cap * kMaxCluster) {
-    const int nc = static_cast<int>((cols + cap - 1) / cap);
-    // equal slices, each a whole number of 16-byte vectors
-    int64_t seg = (cols + nc - 1) / nc;
-    seg = (seg + vec - 1) / vec * vec;
-    const size_t smem = size_t(seg * sizeof(T));
-    cudaError_t e = cudaFuncSetAttribute(softmax_rows_onchip<T, true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSliceBytes);
-    if (e == cudaSuccess && nc > 8)
-      e = cudaFuncSetAttribute(softmax_rows_onchip<T, true>,
-                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cfg.dynamicSmemBytes = 0;
+  if (nc > 8) {
+    cudaError_t e = cudaFuncSetAttribute(softmax_rows_stream<T>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr[0].val.clusterDim.x = nc;
     cfg.gridDim = dim3(static_cast<unsigned>(rows * nc));
-    cfg.dynamicSmemBytes = smem;
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, softmax_rows_onchip<T, true>, &cfg);
-    if (e == cudaSuccess && clusters > 0)
-      return cudaLaunchKernelEx(&cfg, softmax_rows_onchip<T, true>, x, y, cols, seg,
-                                aligned ? 1 : 0, status);
-    // a cluster this large cannot be placed: fall through to the streaming form
-    (void)cudaGetLastError();
+    e = cudaOccupancyMaxActiveClusters(&clusters, softmax_rows_stream<T>, &cfg);
+    if (e != cudaSuccess || clusters == 0) {
+      (void)cudaGetLastError();
+      nc = 8;  // a cluster this large cannot be placed: use the portable size
+    }
   }
-  const int nc = kStreamCluster;
   int64_t seg = (cols + nc - 1) / nc;
   seg = (seg + vec - 1) / vec * vec;
   attr[0].val.clusterDim.x = nc;
   cfg.gridDim = dim3(static_cast<unsigned>(rows * nc));
-  cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, softmax_rows_stream<T>, x, y, cols, seg, aligned ? 1 : 0);
 }
 
