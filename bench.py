@@ -317,30 +317,26 @@ def run_ours(args, dist, rank, world, local):
                               "ms_per_step": ms_step, "roofline": roofline}), flush=True)
         return
 
-    # end to end through the public API with host buffers (fresh device tensors)
-    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    # end to end through the public API with host buffers: rf_attn_fwd_host
+    # copies Q, K, V in and O, LSE out every step, pipelined with its kernels
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
-    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    op = torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory()
+    lp = torch.empty(q_h.shape[:3], dtype=torch.float32).pin_memory()
+    ws = torch.empty(api.attn_fwd_host_workspace_bytes(w["B"], w["H"], w["Hkv"], w["Sq"], w["Sk"],
+                                                       w["d"], q_h.dtype),
+                     dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        api.attn_fwd(q, k, v, scale, w["causal"], None, o, lse)
-        op.copy_(o, non_blocking=True)
-        lp.copy_(lse, non_blocking=True)
+        api.attn_fwd_host(qp, kp, vp, scale, w["causal"], None, op, lp, workspace=ws, device=dev)
 
     n_e2e = max(3, min(args.steps, 50))
     e2e_total, _ = time_steps(e2e_step, n_e2e, 3, stream, dist)
     e2e_total = max_over_ranks(dist, e2e_total)
     e2e_ms = e2e_total / n_e2e
-    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
-    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+    d2h = op.numel() * op.element_size() + lp.numel() * lp.element_size()
 
-    del q, k, v, o, lse, qp, kp, vp, op, lp
+    del qp, kp, vp, op, lp, ws
     torch.cuda.empty_cache()
 
     decode = bench_decode(args, dev, stream, peaks, peak_src)

@@ -132,6 +132,41 @@ rf_status rf_attn_fwd(const void *q, const void *k, const void *v, void *o, floa
                       rf_stream stream);
 
 /*
+ * Attention forward on HOST buffers, the copies overlapped with the kernels.
+ * Computes exactly what rf_attn_fwd computes (same arguments, same results),
+ * but q, k, v are read from and o, lse written to host memory. The work is
+ * cut into chunks of whole (batch, key/value-head group) slices -- independent
+ * problems, so no merge is needed (the single-segment strategy per chunk) --
+ * and chunk c's copy in, its kernel and the copy out of chunk c - 1 run
+ * concurrently on two internal streams and the caller's stream.
+ *  q, k, v, o, lse: host pointers in rf_attn_fwd's layouts; page-locked
+ *      memory (cudaHostAlloc, torch pin_memory) lets the copies run
+ *      asynchronously, pageable memory works but serialises them. lse may be
+ *      NULL. Must not change (q, k, v) or be read (o, lse) until the work on
+ *      `stream` is done.
+ *  ws: device workspace of at least rf_attn_fwd_host_workspace_bytes(...)
+ *      bytes, 256-byte aligned, owned by the caller (two chunks in flight);
+ *      no other call may use it until this one's work on `stream` is done.
+ *  blockmask: as for rf_attn_fwd (device lists).
+ * Ordering: the copies start after the work already queued on `stream`, and
+ * work queued on `stream` afterwards starts after the last copy out; the host
+ * is not blocked (except by pageable copies). The library creates two streams
+ * and a few events per device on first use and keeps them.
+ * Errors: those of rf_attn_fwd; RF_ERR_INVALID for NULL host pointers or a
+ * short or misaligned workspace, or while the visited-tile debug buffer is
+ * set; RF_ERR_CUDA if a copy or stream operation fails.
+ */
+rf_status rf_attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int Hkv, int Sq, int Sk, int d, float scale,
+                           int causal, const rf_blockmask *blockmask, rf_dtype dt, void *ws,
+                           size_t ws_bytes, rf_stream stream);
+
+/* Bytes of device workspace rf_attn_fwd_host needs for these sizes (two
+ * chunks of Q, K, V, O and LSE); 0 for invalid arguments. */
+size_t rf_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int Sq, int Sk, int d,
+                                        rf_dtype dt);
+
+/*
  * Split-K decode (multi-segment strategy; FlashDecoding as a special case).
  * One query row per head: q [B,H,1,d], k/v [B,Hkv,Sk,d], o [B,H,1,d], all
  * dtype dt (RF_BF16); lse [B,H,1] float32 (may be NULL). The keys are cut

@@ -52,6 +52,9 @@ SIGNATURES = {
                                    _P]),
     "rf_attn_decode_splitk_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I,
                                            _P]),
+    "rf_attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
+                              ctypes.POINTER(RFBlockMask), _I, _P, _SZ, _P]),
+    "rf_attn_fwd_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "rf_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "rf_splitk_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P]),
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
@@ -180,6 +183,40 @@ def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=No
     bm = ctypes.byref(blockmask.as_struct()) if blockmask is not None else None
     _check(lib().rf_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Sq, Sk, d,
                              float(scale), 1 if causal else 0, bm, _dt(q), _stream()))
+    return o, lse
+
+
+def attn_fwd_host_workspace_bytes(B, H, Hkv, Sq, Sk, d, dtype=torch.bfloat16):
+    return int(lib().rf_attn_fwd_host_workspace_bytes(
+        B, H, Hkv, Sq, Sk, d, RF_F32 if dtype == torch.float32 else RF_BF16))
+
+
+def attn_fwd_host(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,
+                  with_lse=True, workspace=None, device=None):
+    """rf_attn_fwd_host: q [B,H,Sq,d], k/v [B,Hkv,Sk,d] in HOST memory (pinned for
+    overlap) -> (o, lse) in host memory; copies and kernels pipelined by chunks.
+    The call is asynchronous on the current stream of `device`."""
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous host tensors")
+    B, H, Sq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    pin = q.is_pinned()
+    o = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin) if out is None else out
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, pin_memory=pin)
+    nbytes = attn_fwd_host_workspace_bytes(B, H, Hkv, Sq, Sk, d, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(1, nbytes), dtype=torch.uint8, device=dev)
+    _cuda(workspace)
+    bm = ctypes.byref(blockmask.as_struct()) if blockmask is not None else None
+    with torch.cuda.device(dev):
+        _check(lib().rf_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv,
+                                      Sq, Sk, d, float(scale), 1 if causal else 0, bm, _dt(q),
+                                      _ptr(workspace), workspace.numel(), _stream()))
     return o, lse
 
 

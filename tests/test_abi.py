@@ -147,3 +147,29 @@ def test_softmax_and_blockmask_validation(L):
     assert L.rf_debug_set_visited(A, 0) == api.RF_ERR_INVALID
     assert L.rf_debug_set_visited(None, 0) == api.RF_OK
     assert L.rf_device_status(None, None) == api.RF_ERR_INVALID
+
+
+def _attn_host(L, q=A, k=A, v=A, o=A, lse=A, B=2, H=4, Hkv=2, Sq=256, Sk=256, d=128, ws=0x20000,
+               ws_bytes=None, dt=api.RF_BF16):
+    if ws_bytes is None:
+        ws_bytes = L.rf_attn_fwd_host_workspace_bytes(B, H, Hkv, Sq, Sk, d, dt)
+    return L.rf_attn_fwd_host(q, k, v, o, lse, B, H, Hkv, Sq, Sk, d, 0.1, 0, None, dt, ws,
+                              ws_bytes, None)
+
+
+def test_attn_fwd_host_workspace_size(L):
+    # two chunks in flight, each 256-byte aligned Q, K, V, O and LSE of one
+    # (batch, kv-head group) slice: B = 2 -> 4 chunks per batch element -> 1 kv head
+    n = L.rf_attn_fwd_host_workspace_bytes(2, 4, 4, 256, 512, 128, api.RF_BF16)
+    slot = 256 * 128 * 2 + 2 * 512 * 128 * 2 + 256 * 128 * 2 + 256 * 4
+    assert n == 2 * slot
+    assert L.rf_attn_fwd_host_workspace_bytes(0, 4, 4, 256, 512, 128, api.RF_BF16) == 0
+    assert L.rf_attn_fwd_host_workspace_bytes(1, 4, 3, 256, 512, 128, api.RF_BF16) == 0
+    assert L.rf_attn_fwd_host_workspace_bytes(1, 4, 4, 256, 512, 128, 7) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=0), dict(Hkv=3), dict(dt=9), dict(q=None), dict(k=None), dict(o=None),
+    dict(ws=None), dict(ws=0x20008), dict(ws_bytes=1024)])
+def test_attn_fwd_host_rejects(L, kw):
+    assert _attn_host(L, **kw) == api.RF_ERR_INVALID

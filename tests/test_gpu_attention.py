@@ -140,3 +140,31 @@ def test_malformed_block_list_is_reported(cuda_device):
         api.device_status()
     assert e.value.status == api.RF_ERR_INVALID
     assert api.device_status() == 0     # reading clears it
+
+
+@pytest.mark.parametrize("B,H,Hkv,Sq,Sk,d,causal,dtype,use_tm,with_lse", [
+    (8, 4, 2, 300, 500, 128, True, "bf16", False, True),     # whole batch elements per chunk
+    (1, 8, 8, 257, 257, 64, False, "bf16", False, True),     # one kv head per chunk
+    (2, 6, 3, 200, 640, 128, True, "bf16", True, True),      # GQA + per-head block lists
+    (3, 2, 1, 129, 70, 64, False, "f32", False, False),      # SIMT path, no LSE
+    (2, 4, 2, 150, 0, 128, False, "bf16", False, True),      # no keys
+])
+def test_attn_fwd_host_equals_device(cuda_device, B, H, Hkv, Sq, Sk, d, causal, dtype, use_tm,
+                                     with_lse):
+    """The host-buffer entry point computes exactly what rf_attn_fwd computes:
+    per-chunk launches do the same per-row work, so results are bit-identical."""
+    q, k, v = inputs.make_qkv(B, H, Hkv, Sq, Sk, d, 17, dtype)
+    bm = None
+    if use_tm:
+        tm = inputs.random_tile_mask(inputs.n_tiles(Sq), inputs.n_tiles(Sk), 0.5, 5, nheads=B * H)
+        bm = api.BlockMask.from_dense(tm)
+    o_d, lse_d = api.attn_fwd(q.cuda(), k.cuda(), v.cuda(), None, causal, bm)
+    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_h, lse_h = api.attn_fwd_host(qp, kp, vp, None, causal, bm, with_lse=with_lse)
+    torch.cuda.current_stream().synchronize()
+    assert api.device_status() == 0
+    assert torch.equal(o_h, o_d.cpu())
+    if with_lse:
+        assert torch.equal(lse_h, lse_d.cpu())
+    else:
+        assert lse_h is None
