@@ -48,6 +48,11 @@ TRAFFIC = {
     # (sources since then differ only by device helpers the kernel does not use)
     "attn_tc_mha_prefill": {"digest": "6d1502890a710a2a", "bytes": 517469184,
                             "sources": ("attn_tc.cu", "rf_device.cuh")},
+    # softmax_rows kernels: dram__bytes.sum.per_second x duration
+    "softmax_rows_64k": {"digest": "2e0e34e6b5aed013", "bytes": 2089064000,
+                         "sources": ("softmax_rows.cu", "rf_device.cuh")},
+    "softmax_rows_1m": {"digest": "2e0e34e6b5aed013", "bytes": 2089842000,
+                        "sources": ("softmax_rows.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
     # (sources since then differ only by device helpers the kernel does not use)
     "decode_partials_decode_splitk": {"digest": "4c12c369bc05677a", "bytes": 4302000000,
@@ -427,7 +432,8 @@ def bench_softmax(args, dev, stream, peaks, peak_src, name="rows_64k"):
            "unit": "GB/s", "ms_per_step": ms,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"], "frac_of_8TBs": gbs / 8000.0,
-                        "traffic": None, "peak_source": "%s HBM copy" % peak_src}}
+                        "traffic": traffic_for("softmax_" + name),
+                        "peak_source": "%s HBM copy" % peak_src}}
     del x, y
     torch.cuda.empty_cache()
     return out
