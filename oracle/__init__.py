@@ -14,8 +14,10 @@ Modules
 -------
 ``three_pass``   three-pass safe-softmax attention, row softmax, split-K
                  partials and their log-sum-exp merge, the set of tiles that
-                 hold at least one visible (query, key) pair, and the
-                 block-sparse row lists of a tile mask.
+                 hold at least one visible (query, key) pair, the
+                 block-sparse row lists of a tile mask, and the two-level
+                 (outer lists + inner 8x8 bitmaps) encoding of an element
+                 mask.
 ``incremental``  an independent float64 run of the incremental (online) form,
                  used only to check that the derivation the GPU follows
                  reaches the three-pass result.
@@ -33,6 +35,8 @@ from .three_pass import (  # noqa: F401
     merge_partials,
     softmax_rows,
     split_bounds,
+    two_level_decode,
+    two_level_encode,
     visible_mask,
     visited_tiles,
 )

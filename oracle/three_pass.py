@@ -19,7 +19,9 @@ Sources (page title, section):
 * Accelerating Sparse Transformer Inference on GPU (STOF) -- technical
   summary, "Méthodologie", unified MHA module: block-sparse outer tiles kept
   as row-compressed (BSR) lists; masked tiles are skipped entirely
-  ("Énoncé du problème").
+  ("Énoncé du problème"). Same section, two-level storage format: outer
+  tiles are "full" (every element valid) or "partial"; the valid elements of
+  a partial tile are kept as one 64-bit bitmap per 8x8 inner block.
 
 The oracle deliberately does NOT use the incremental (online) form the GPU
 uses; it runs the definition: pass 1 row maximum, pass 2 sum of shifted
@@ -36,6 +38,14 @@ Readings where the pages are silent (each listed in the design notes):
 * GQA: query head h reads key/value head h // (H // Hkv).
 * A row with no visible key gives O = 0 and LSE = -inf.
 * A row-softmax row whose entries are all -inf gives y = 0.
+* An element mask is a bool array over (query row, key); a key is visible
+  only if the element mask allows it as well as the tile mask and causality.
+* Two-level format (the pages give no bit order): an outer tile is listed if
+  it holds a valid element; it is full if every element of it that lies
+  inside the Sq x Sk matrix is valid, else partial. The 16 x 16 inner blocks
+  of a partial tile are stored row-major, 256 words per tile; bit 8 r + c of
+  a word is element (r, c) of its 8 x 8 block (row-major bits). Elements
+  outside the matrix have bit 0.
 * Split-K: contiguous splits of Sk // nsplit keys, the last split taking the
   remainder.
 """
@@ -52,11 +62,12 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def visible_mask(Sq, Sk, causal, tile_mask=None, tile=128, rows=None):
+def visible_mask(Sq, Sk, causal, tile_mask=None, tile=128, rows=None, elem_mask=None):
     """bool [R, Sk]: True where query row i may attend key j.
 
     ``rows`` selects query rows (default: all Sq rows). ``tile_mask`` is a
-    2-D bool array [ceil(Sq/tile), ceil(Sk/tile)] for one head.
+    2-D bool array [ceil(Sq/tile), ceil(Sk/tile)] for one head;
+    ``elem_mask`` a 2-D bool array [Sq, Sk] for one head.
     """
     rows = np.arange(Sq, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
     i = rows[:, None]
@@ -67,10 +78,13 @@ def visible_mask(Sq, Sk, causal, tile_mask=None, tile=128, rows=None):
     if tile_mask is not None:
         tm = np.asarray(tile_mask, dtype=bool)
         vis &= tm[i // tile, j // tile]
+    if elem_mask is not None:
+        vis &= np.asarray(elem_mask, dtype=bool)[rows]
     return vis
 
 
 def _head_tile_mask(tile_mask, b, h, H):
+    """The mask of head (b, h): a 2-D mask is shared, a 3-D one is per head."""
     if tile_mask is None:
         return None
     tm = np.asarray(tile_mask, dtype=bool)
@@ -103,12 +117,14 @@ def _three_pass(q, k, v, scale, vis):
     return o, lse
 
 
-def attention(q, k, v, scale, causal=False, tile_mask=None, tile=128, rows=None, heads=None):
+def attention(q, k, v, scale, causal=False, tile_mask=None, tile=128, rows=None, heads=None,
+              elem_mask=None):
     """Safe-softmax attention, float64, plain definition.
 
     q [B, H, Sq, d]; k, v [B, Hkv, Sk, d(v)]; any float dtype (cast exactly
     to float64). ``tile_mask``: None, bool [nqt, nkt] shared by all heads, or
-    bool [B*H, nqt, nkt] per head. ``rows``: query-row indices to compute
+    bool [B*H, nqt, nkt] per head. ``elem_mask``: None, bool [Sq, Sk] shared
+    or [B*H, Sq, Sk] per head. ``rows``: query-row indices to compute
     (default all). ``heads``: list of (b, h) to compute (default all).
 
     Returns (o, lse): with ``heads`` None, o [B, H, R, dv] and lse [B, H, R];
@@ -128,10 +144,11 @@ def attention(q, k, v, scale, causal=False, tile_mask=None, tile=128, rows=None,
     lse = np.full((len(hl), rows.size), NEG_INF)
     for n, (b, h) in enumerate(hl):
         tm = _head_tile_mask(tile_mask, b, h, H)
+        em = _head_tile_mask(elem_mask, b, h, H)
         kv = h // G
         for r0 in range(0, rows.size, ROW_BLOCK):
             rr = rows[r0:r0 + ROW_BLOCK]
-            vis = visible_mask(Sq, Sk, causal, tm, tile, rr)
+            vis = visible_mask(Sq, Sk, causal, tm, tile, rr, em)
             o[n, r0:r0 + rr.size], lse[n, r0:r0 + rr.size] = _three_pass(
                 q[b, h, rr], k[b, kv], v[b, kv], scale, vis)
     if all_heads:
@@ -214,17 +231,18 @@ def merge_partials(o_part, lse_part):
     return o, lse
 
 
-def visited_tiles(Sq, Sk, causal, tile_mask=None, tile=128):
+def visited_tiles(Sq, Sk, causal, tile_mask=None, tile=128, elem_mask=None):
     """bool [nqt, nkt]: tiles holding at least one visible (query, key) pair.
 
     This is the set of tiles a kernel that skips masked tiles must process
-    (and the only ones it may process). ``tile_mask`` is 2-D (one head).
+    (and the only ones it may process). ``tile_mask`` and ``elem_mask`` are
+    2-D (one head).
     """
     nqt, nkt = -(-Sq // tile), -(-Sk // tile)
     out = np.zeros((nqt, nkt), dtype=bool)
     for qt in range(nqt):
         rows = np.arange(qt * tile, min(Sq, (qt + 1) * tile))
-        vis = visible_mask(Sq, Sk, causal, tile_mask, tile, rows)
+        vis = visible_mask(Sq, Sk, causal, tile_mask, tile, rows, elem_mask)
         colany = vis.any(axis=0)
         for kt in range(nkt):
             out[qt, kt] = colany[kt * tile:(kt + 1) * tile].any()
@@ -246,3 +264,69 @@ def bsr_from_tile_mask(tile_mask):
     cols = [np.nonzero(r)[0] for r in flat]
     col_idx = np.concatenate(cols).astype(np.int32) if cols else np.zeros(0, np.int32)
     return row_ptr, col_idx
+
+
+def two_level_encode(elem_mask, tile=128, inner=8):
+    """STOF's two-level storage of an element mask (outer BSR + inner bitmaps).
+
+    elem_mask: bool [nheads, Sq, Sk] or [Sq, Sk]. For each head and each row
+    of outer tiles, the tiles that hold a valid element are listed in
+    ascending column order (row_ptr, col_idx, as ``bsr_from_tile_mask``);
+    tile_bits[n] is -1 for a full tile, else the index of its bitmap block
+    in ``bits``, which holds (tile // inner)**2 words per partial tile:
+    inner blocks row-major, bit inner*r + c of a word = element (r, c) of
+    its block.
+    Returns (row_ptr int32, col_idx int32, tile_bits int32, bits uint64 [P, nb*nb]).
+    """
+    em = np.asarray(elem_mask, dtype=bool)
+    if em.ndim == 2:
+        em = em[None]
+    nh, Sq, Sk = em.shape
+    nqt, nkt, nb = -(-Sq // tile), -(-Sk // tile), tile // inner
+    weights = np.left_shift(np.uint64(1), np.arange(inner * inner, dtype=np.uint64))
+    row_ptr, col_idx, tile_bits, bits = [0], [], [], []
+    for h in range(nh):
+        for qt in range(nqt):
+            for kt in range(nkt):
+                blk = em[h, qt * tile:(qt + 1) * tile, kt * tile:(kt + 1) * tile]
+                if not blk.any():
+                    continue
+                col_idx.append(kt)
+                if blk.all():
+                    tile_bits.append(-1)
+                    continue
+                full = np.zeros((tile, tile), dtype=bool)   # outside the matrix: 0
+                full[:blk.shape[0], :blk.shape[1]] = blk
+                # [br, r, bc, c] -> [br, bc, r * inner + c]
+                cells = full.reshape(nb, inner, nb, inner).transpose(0, 2, 1, 3)
+                cells = cells.reshape(nb * nb, inner * inner)
+                words = (cells.astype(np.uint64) * weights).sum(axis=1, dtype=np.uint64)
+                tile_bits.append(len(bits))
+                bits.append(words)
+            row_ptr.append(len(col_idx))
+    bits = np.stack(bits) if bits else np.zeros((0, nb * nb), np.uint64)
+    return (np.asarray(row_ptr, np.int32), np.asarray(col_idx, np.int32),
+            np.asarray(tile_bits, np.int32), bits.astype(np.uint64))
+
+
+def two_level_decode(row_ptr, col_idx, tile_bits, bits, nheads, Sq, Sk, tile=128, inner=8):
+    """The element mask [nheads, Sq, Sk] that a two-level encoding describes."""
+    nqt, nkt, nb = -(-Sq // tile), -(-Sk // tile), tile // inner
+    out = np.zeros((nheads, nqt * tile, nkt * tile), dtype=bool)
+    for h in range(nheads):
+        for qt in range(nqt):
+            r = h * nqt + qt
+            for n in range(row_ptr[r], row_ptr[r + 1]):
+                kt = col_idx[n]
+                dst = out[h, qt * tile:(qt + 1) * tile, kt * tile:(kt + 1) * tile]
+                if tile_bits[n] < 0:
+                    dst[:] = True
+                    continue
+                for blk in range(nb * nb):
+                    br, bc = divmod(blk, nb)
+                    w = int(bits[tile_bits[n], blk])
+                    for e in range(inner * inner):
+                        if (w >> e) & 1:
+                            rr, cc = divmod(e, inner)
+                            dst[br * inner + rr, bc * inner + cc] = True
+    return out[:, :Sq, :Sk]

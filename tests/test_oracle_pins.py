@@ -58,10 +58,16 @@ def _close(a, b, tol=TOL):
 # brute force with Python math
 
 
-def _brute_visible(Sq, Sk, causal, tm, tile):
+def _brute_visible(Sq, Sk, causal, tm, tile, em=None):
     """Visibility by explicit loops: bottom-right causal means the last query
-    row sees every key and each earlier row one key fewer."""
+    row sees every key and each earlier row one key fewer; an element mask
+    removes single keys."""
     vis = [[True] * Sk for _ in range(Sq)]
+    if em is not None:
+        for i in range(Sq):
+            for j in range(Sk):
+                if not em[i][j]:
+                    vis[i][j] = False
     for i in range(Sq):
         if causal:
             n_seen = Sk - (Sq - 1 - i)          # keys seen by row i
@@ -95,7 +101,7 @@ def _brute_head(q, k, v, scale, vis):
     return o, lse
 
 
-def _brute_attention(q, k, v, scale, causal=False, tm=None, tile=2):
+def _brute_attention(q, k, v, scale, causal=False, tm=None, tile=2, em=None):
     B, H, Sq, _ = q.shape
     _, Hkv, Sk, _ = k.shape
     G = H // Hkv
@@ -104,7 +110,8 @@ def _brute_attention(q, k, v, scale, causal=False, tm=None, tile=2):
     for b in range(B):
         for h in range(H):
             tmh = None if tm is None else (tm if tm.ndim == 2 else tm[b * H + h])
-            vis = _brute_visible(Sq, Sk, causal, None if tmh is None else tmh.tolist(), tile)
+            emh = None if em is None else (em if em.ndim == 2 else em[b * H + h]).tolist()
+            vis = _brute_visible(Sq, Sk, causal, None if tmh is None else tmh.tolist(), tile, emh)
             ob, lb = _brute_head(q[b, h].tolist(), k[b, h // G].tolist(), v[b, h // G].tolist(),
                                  scale, vis)
             o[b, h], lse[b, h] = ob, lb
@@ -120,6 +127,74 @@ BRUTE_CASES = [
     (2, 3, 3, 7, 8, 4, False, True),
     (1, 2, 1, 8, 8, 3, True, True),
 ]
+
+
+@pytest.mark.parametrize("causal,per_head", [(False, False), (True, True)])
+def test_brute_force_element_mask(causal, per_head):
+    """Attention under an element mask (STOF's inner level) equals explicit
+    loops that drop every masked (query, key) pair."""
+    B, H, Hkv, Sq, Sk, d = 1, 2, 1, 6, 7, 3
+    q, k, v = _rand((B, H, Sq, d), 11), _rand((B, Hkv, Sk, d), 12), _rand((B, Hkv, Sk, d), 13)
+    rng = np.random.default_rng(14)
+    em = rng.random((B * H, Sq, Sk) if per_head else (Sq, Sk)) < 0.5
+    o, lse = oracle.attention(q, k, v, 0.9, causal, elem_mask=em)
+    ob, lb = _brute_attention(q, k, v, 0.9, causal, None, 2, em)
+    _close(o, ob)
+    _close(lse, lb)
+
+
+def test_element_mask_special_cases():
+    """An all-true element mask changes nothing; one that is constant over
+    each tile is the same as the tile mask."""
+    B, H, Sq, Sk, d, tile = 1, 2, 9, 10, 4, 3
+    q, k, v = _rand((B, H, Sq, d), 21), _rand((B, H, Sk, d), 22), _rand((B, H, Sk, d), 23)
+    base = oracle.attention(q, k, v, 0.5, True)
+    allt = oracle.attention(q, k, v, 0.5, True, elem_mask=np.ones((Sq, Sk), bool))
+    _close(allt[0], base[0])
+    _close(allt[1], base[1])
+    tm = np.random.default_rng(24).random((-(-Sq // tile), -(-Sk // tile))) < 0.5
+    em = np.repeat(np.repeat(tm, tile, 0), tile, 1)[:Sq, :Sk]
+    a = oracle.attention(q, k, v, 0.5, False, tm, tile)
+    b = oracle.attention(q, k, v, 0.5, False, elem_mask=em)
+    _close(a[0], b[0])
+    _close(a[1], b[1])
+
+
+def test_two_level_format_examples():
+    """The words the pages describe: one uint64 per 8x8 inner block of a
+    partial outer tile (bit 8r + c = element (r, c), the reading taken);
+    full tiles carry no bitmap; a tile with no valid element is not listed."""
+    m = np.zeros((1, 256, 384), bool)
+    m[0, 0, :8] = True                 # tile (0,0): first row of inner block (0,0)
+    m[0, 9, 16] = True                 # tile (0,0): inner block (1,2), element (1,0)
+    m[0, 128:, 256:] = True            # tile (1,2): full
+    m[0, 130, 131] = True              # tile (1,1): inner block (0,0), element (2,3)
+    rp, ci, tb, bits = oracle.two_level_encode(m)
+    assert rp.tolist() == [0, 1, 3] and ci.tolist() == [0, 1, 2] and tb.tolist() == [0, 1, -1]
+    w0 = bits[0]
+    assert int(w0[0]) == 0xFF and int(w0[1 * 16 + 2]) == 1 << 8
+    assert np.count_nonzero(w0) == 2
+    assert int(bits[1][0]) == 1 << (2 * 8 + 3) and np.count_nonzero(bits[1]) == 1
+    # a block whose 64 elements are all valid is the all-ones word
+    m2 = np.zeros((1, 128, 128), bool)
+    m2[0, 8:16, 16:24] = True
+    assert int(oracle.two_level_encode(m2)[3][0][1 * 16 + 2]) == 0xFFFFFFFFFFFFFFFF
+
+
+@pytest.mark.parametrize("shape,density", [((2, 300, 200), 0.02), ((1, 129, 257), 0.5),
+                                           ((3, 64, 64), 0.9)])
+def test_two_level_round_trip(shape, density):
+    rng = np.random.default_rng(int(density * 100) + shape[1])
+    m = rng.random(shape) < density
+    m[0, :, :64] = True                # whole tiles valid: listed as full
+    rp, ci, tb, bits = oracle.two_level_encode(m)
+    assert (oracle.two_level_decode(rp, ci, tb, bits, *shape) == m).all()
+    # listed tiles are exactly the tiles holding a valid element
+    tiles = np.zeros((shape[0], -(-shape[1] // 128), -(-shape[2] // 128)), bool)
+    for h, i, j in zip(*np.nonzero(m)):
+        tiles[h, i // 128, j // 128] = True
+    rp2, ci2 = oracle.bsr_from_tile_mask(tiles)
+    assert np.array_equal(rp, rp2) and np.array_equal(ci, ci2)
 
 
 @pytest.mark.parametrize("case", BRUTE_CASES)
@@ -516,15 +591,20 @@ _orig_three_pass = oa._three_pass
 _orig_visible = oa.visible_mask
 
 
-def _mutant_top_left(Sq, Sk, causal, tile_mask=None, tile=128, rows=None):
-    vis = _orig_visible(Sq, Sk, False, tile_mask, tile, rows)
+def _mutant_top_left(Sq, Sk, causal, tile_mask=None, tile=128, rows=None, elem_mask=None):
+    vis = _orig_visible(Sq, Sk, False, tile_mask, tile, rows, elem_mask)
     if causal:
         rows = np.arange(Sq) if rows is None else np.asarray(rows)
         vis &= np.arange(Sk)[None, :] <= rows[:, None]
     return vis
 
 
+def _mutant_no_elem_mask(Sq, Sk, causal, tile_mask=None, tile=128, rows=None, elem_mask=None):
+    return _orig_visible(Sq, Sk, causal, tile_mask, tile, rows)
+
+
 def _pins():
+    yield lambda: test_brute_force_element_mask(True, True)
     yield lambda: test_brute_force_tiny(BRUTE_CASES[1])
     yield lambda: test_brute_force_tiny(BRUTE_CASES[3])
     yield test_closed_form_one_row
@@ -535,7 +615,7 @@ def _pins():
 @pytest.mark.parametrize("target,mutant", [
     ("_three_pass", _mutant_no_scale), ("_three_pass", _mutant_log2),
     ("_three_pass", _mutant_transposed_v), ("_three_pass", _mutant_no_normalise),
-    ("visible_mask", _mutant_top_left)])
+    ("visible_mask", _mutant_top_left), ("visible_mask", _mutant_no_elem_mask)])
 def test_pins_catch_planted_mistakes(monkeypatch, target, mutant):
     monkeypatch.setattr(oa, target, mutant)
     failures = 0
