@@ -79,17 +79,27 @@ typedef enum {
  *  per_head = 0: one list set shared by every (b, h); row_ptr has nqt + 1 entries.
  *  per_head = 1: B*H list sets back to back, head n = b * H + h;
  *                row_ptr has B*H*nqt + 1 entries.
- * row_ptr and col_idx are device pointers (int32) owned by the caller; the
- * struct itself is read on the host during the call only.
+ * Inner level (the same page's two-level format, optional): with tile_bits
+ * non-NULL, tile_bits[n] (int32, parallel to col_idx) is -1 for a full tile
+ * and otherwise the index P of the tile's bitmaps, bits[256 P .. 256 P + 255]:
+ * one uint64 per 8 x 8 inner block, blocks row-major over the tile's 16 x 16,
+ * bit 8 r + c = element (r, c) of the block (1 = attended). A partial tile is
+ * attended only where its bit is set (and, with causal, causally visible).
+ * tile_bits = NULL: every listed tile is full (bits is ignored).
+ * row_ptr, col_idx, tile_bits and bits are device pointers owned by the
+ * caller; the struct itself is read on the host during the call only.
+ * Zero-initialise the struct so that fields added later read as absent.
  */
 typedef struct {
-  int tile_q;              /* must be 128 */
-  int tile_k;              /* must be 128 */
-  int nqt;                 /* must be ceil(Sq / 128) */
-  int nkt;                 /* must be ceil(Sk / 128) */
-  const int32_t *row_ptr;  /* device */
-  const int32_t *col_idx;  /* device */
-  int per_head;            /* 0 or 1 */
+  int tile_q;                /* must be 128 */
+  int tile_k;                /* must be 128 */
+  int nqt;                   /* must be ceil(Sq / 128) */
+  int nkt;                   /* must be ceil(Sk / 128) */
+  const int32_t *row_ptr;    /* device */
+  const int32_t *col_idx;    /* device */
+  int per_head;              /* 0 or 1 */
+  const int32_t *tile_bits;  /* device, parallel to col_idx; NULL: all tiles full */
+  const uint64_t *bits;      /* device, 256 words per partial tile */
 } rf_blockmask;
 
 /*
@@ -242,6 +252,28 @@ rf_status rf_splitk_merge(const float *o_part, const float *lse_part, void *o, f
 rf_status rf_blockmask_build(const uint8_t *dense, int nheads, int nqt, int nkt,
                              int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
                              rf_stream stream);
+
+/*
+ * Build the two-level (outer lists + inner 8 x 8 bitmaps) mask of a dense
+ * element mask on the device (STOF page, two-level storage format).
+ *  dense: uint8 [nheads, Sq, Sk] (nonzero = attend), device.
+ *  An outer 128 x 128 tile is listed if it holds a nonzero element; it is
+ *  full (tile_bits = -1) if every element of it inside the Sq x Sk matrix is
+ *  nonzero, else partial, with 256 bitmap words (bits outside the matrix 0).
+ *  row_ptr: int32 [nheads*nqt + 1]; col_idx, tile_bits: int32 [nheads*nqt*nkt]
+ *  (capacity for every tile; entries past row_ptr[last] are unspecified);
+ *  bits: uint64 [bits_cap * 256], partial tiles numbered in list order; a
+ *  mask with more than bits_cap partial tiles records RF_ERR_INVALID in the
+ *  device status word and leaves the extra bitmaps unwritten. bits = NULL:
+ *  only the lists are built (tile_bits still numbers the partial tiles), no
+ *  error is recorded, and n_partial tells how large bits must be. n_partial
+ *  (device int32, may be NULL) receives the number of partial tiles.
+ * nheads, Sq, Sk >= 1, bits_cap >= 0; nqt = ceil(Sq/128), nkt = ceil(Sk/128).
+ */
+rf_status rf_blockmask_build_elements(const uint8_t *dense, int nheads, int Sq, int Sk,
+                                      int32_t *row_ptr, int32_t *col_idx, int32_t *tile_bits,
+                                      uint64_t *bits, int64_t bits_cap, int32_t *n_partial,
+                                      rf_stream stream);
 
 /*
  * Test aid: when visited is non-NULL, every later rf_attn_fwd on this host

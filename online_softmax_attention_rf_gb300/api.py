@@ -32,7 +32,8 @@ class RFError(RuntimeError):
 class RFBlockMask(ctypes.Structure):
     _fields_ = [("tile_q", ctypes.c_int), ("tile_k", ctypes.c_int), ("nqt", ctypes.c_int),
                 ("nkt", ctypes.c_int), ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p),
-                ("per_head", ctypes.c_int)]
+                ("per_head", ctypes.c_int), ("tile_bits", ctypes.c_void_p),
+                ("bits", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -58,6 +59,7 @@ SIGNATURES = {
     "rf_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "rf_splitk_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P]),
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
+    "rf_blockmask_build_elements": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
     "rf_debug_set_visited": (_I, [_P, _I64]),
     "rf_device_status": (_I, [_P, ctypes.POINTER(_I)]),
     "rf_last_error": (ctypes.c_char_p, []),
@@ -122,16 +124,43 @@ class BlockMask:
     """Block-sparse 128 x 128 tile lists resident on the device.
 
     ``row_ptr`` int32 [nheads*nqt + 1] and ``col_idx`` int32 [capacity];
-    ``per_head`` is 1 when each (batch, head) has its own lists.
+    ``per_head`` is 1 when each (batch, head) has its own lists. With the
+    two-level form, ``tile_bits`` int32 (parallel to ``col_idx``, -1 = full
+    tile) and ``bits`` uint64 viewed as int64 [partial tiles, 256].
     """
 
-    def __init__(self, row_ptr, col_idx, nqt, nkt, per_head):
+    def __init__(self, row_ptr, col_idx, nqt, nkt, per_head, tile_bits=None, bits=None):
         self.row_ptr, self.col_idx = row_ptr, col_idx
         self.nqt, self.nkt, self.per_head = nqt, nkt, per_head
+        self.tile_bits, self.bits = tile_bits, bits
 
     def as_struct(self):
         return RFBlockMask(TILE, TILE, self.nqt, self.nkt, self.row_ptr.data_ptr(),
-                           self.col_idx.data_ptr(), self.per_head)
+                           self.col_idx.data_ptr(), self.per_head,
+                           self.tile_bits.data_ptr() if self.tile_bits is not None else None,
+                           self.bits.data_ptr() if self.bits is not None else None)
+
+    @classmethod
+    def from_dense_elements(cls, elem_mask, device="cuda"):
+        """Two-level lists (outer tiles + inner 8x8 bitmaps) from a bool/uint8
+        element mask [Sq, Sk] (shared) or [nheads, Sq, Sk] (per head), built
+        on the device (rf_blockmask_build_elements; a first pass counts the
+        partial tiles to size the bitmaps)."""
+        em = torch.as_tensor(elem_mask)
+        per_head = 1 if em.dim() == 3 else 0
+        if em.dim() == 2:
+            em = em.unsqueeze(0)
+        nheads, Sq, Sk = em.shape
+        dense = em.to(device=device, dtype=torch.uint8).contiguous()
+        nqt, nkt = -(-Sq // TILE), -(-Sk // TILE)
+        row_ptr = torch.empty(nheads * nqt + 1, dtype=torch.int32, device=device)
+        col_idx = torch.empty(nheads * nqt * nkt, dtype=torch.int32, device=device)
+        tile_bits = torch.empty(nheads * nqt * nkt, dtype=torch.int32, device=device)
+        n_partial = torch.zeros(1, dtype=torch.int32, device=device)
+        blockmask_build_elements(dense, row_ptr, col_idx, tile_bits, None, n_partial)
+        bits = torch.empty((max(1, int(n_partial.item())), 256), dtype=torch.int64, device=device)
+        blockmask_build_elements(dense, row_ptr, col_idx, tile_bits, bits, n_partial)
+        return cls(row_ptr, col_idx, nqt, nkt, per_head, tile_bits, bits)
 
     @classmethod
     def from_dense(cls, tile_mask, device="cuda"):
@@ -155,6 +184,17 @@ def blockmask_build(dense_u8, row_ptr, col_idx):
     nheads, nqt, nkt = dense_u8.shape
     _check(lib().rf_blockmask_build(_ptr(dense_u8), nheads, nqt, nkt, _ptr(row_ptr),
                                     _ptr(col_idx), col_idx.numel(), _stream()))
+
+
+def blockmask_build_elements(dense_u8, row_ptr, col_idx, tile_bits, bits, n_partial=None):
+    """rf_blockmask_build_elements on [nheads, Sq, Sk] uint8 (in place); ``bits``
+    None builds the lists only (and counts the partial tiles into n_partial)."""
+    _cuda(dense_u8, row_ptr, col_idx, tile_bits, bits, n_partial)
+    nheads, Sq, Sk = dense_u8.shape
+    cap = 0 if bits is None else bits.shape[0]
+    _check(lib().rf_blockmask_build_elements(_ptr(dense_u8), nheads, Sq, Sk, _ptr(row_ptr),
+                                             _ptr(col_idx), _ptr(tile_bits), _ptr(bits), cap,
+                                             _ptr(n_partial), _stream()))
 
 
 def softmax_rows(x, out=None):

@@ -11,7 +11,9 @@
 // no inter-warp synchronisation enters the arithmetic. The eight warps of a
 // CTA share 32-key K/V sub-tiles staged in shared memory. Masked 128 x 128
 // tiles are skipped entirely: the CTA walks the same tile list (dense range,
-// causal range, or block-sparse row) the tensor-core kernel walks.
+// causal range, or block-sparse row) the tensor-core kernel walks; inside a
+// partial tile of a two-level mask each key's bit in its 8 x 8 inner block
+// decides (STOF, two-level storage format).
 #include "rf_device.cuh"
 
 namespace rf {
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArg
     if (int64_t(kt) * kTile >= kend) break;  // beyond every causal row: ascending list ends
     if (a.visited != nullptr && threadIdx.x == 0)
       a.visited[(int64_t(bh) * a.nqt + qt) * a.nkt + kt] = 1;
+    // a partial tile of a two-level mask: its inner 8 x 8 bitmaps decide
+    const int pb = (cols != nullptr && a.tile_bits != nullptr) ? a.tile_bits[n] : -1;
     for (int sub = 0; sub < kTile / kSub; ++sub) {
       const int k0 = kt * kTile + sub * kSub;
       if (k0 >= kend) break;
@@ -114,7 +118,13 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArg
       // scores of this row against the 32 keys (lane j <-> key k0 + j)
       const int key = k0 + lane;
       float s = kNegInf;
-      if (key < row_kend) {
+      bool vis = key < row_kend;
+      if (vis && pb >= 0) {
+        const int rr = i - qt * kTile, cc = key - kt * kTile;
+        const uint64_t w = a.bits[int64_t(pb) * 256 + (rr >> 3) * (kTile / 8) + (cc >> 3)];
+        vis = (w >> ((rr & 7) * 8 + (cc & 7))) & 1;
+      }
+      if (vis) {
         float dot = 0.f;
         const float* qr = Qs + warp * d;
         const float* kr = Ks + lane * dp;

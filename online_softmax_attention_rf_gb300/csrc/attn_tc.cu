@@ -9,7 +9,8 @@
 // Metodologia item 2), the running sum and accumulator are rescaled by
 // exp(m_old - m_new) (item 3), and the head dimension is one tile (item 4).
 // Masked 128 x 128 tiles are never visited (STOF, Méthodologie: block-sparse
-// outer tiles in row-compressed lists; skipped, not zeroed).
+// outer tiles in row-compressed lists; skipped, not zeroed); inside a partial
+// tile of the two-level format the 8 x 8 inner bitmaps mask single keys.
 //
 // Each CTA runs two work items back to back; an item is two 128-row query
 // tiles of one (batch, head) sharing one K/V stream, and a CTA pairs a heavy
@@ -118,7 +119,9 @@ struct Bars {
 struct TileList {
   const int32_t* cols;  // nullptr: range [0, n)
   int n;                // entries (after causal truncation and validation)
+  const int32_t* tb;    // inner-level bitmap index per entry (-1: full); nullptr: all full
   __device__ __forceinline__ int at(int i) const { return cols ? cols[i] : i; }
+  __device__ __forceinline__ int bitmap(int i) const { return tb ? tb[i] : -1; }
 };
 
 struct Params {
@@ -127,6 +130,8 @@ struct Params {
   int causal;
   const int32_t* row_ptr;
   const int32_t* col_idx;
+  const int32_t* tile_bits;  // two-level mask: bitmap index per list entry, or nullptr
+  const uint64_t* bits;      // 256 words (8 x 8 blocks) per partial tile
   int per_head, nqt, nkt, pairs;
   __nv_bfloat16* o;
   float* lse;
@@ -138,7 +143,7 @@ struct Params {
 // Block-sparse rows are truncated at the first entry that is out of range, not
 // strictly ascending, or beyond the last causally visible key.
 __device__ TileList tile_list(const Params& p, int bh, int qt, bool record) {
-  TileList L{nullptr, 0};
+  TileList L{nullptr, 0, nullptr};
   if (qt >= p.nqt) return L;
   const int64_t q_end = min64(p.Sq, int64_t(qt + 1) * kBM);
   const int64_t kend = p.causal ? min64(p.Sk, q_end + (int64_t(p.Sk) - p.Sq)) : p.Sk;
@@ -151,6 +156,7 @@ __device__ TileList tile_list(const Params& p, int bh, int qt, bool record) {
   const int32_t* rp = p.row_ptr + (p.per_head ? int64_t(bh) * p.nqt : 0) + qt;
   const int beg = rp[0], end = rp[1];
   L.cols = p.col_idx + beg;
+  L.tb = p.tile_bits != nullptr ? p.tile_bits + beg : nullptr;
   int n = 0, prev = -1;
   for (int i = beg; i < end; ++i) {
     const int c = p.col_idx[i];
@@ -278,7 +284,9 @@ __device__ __forceinline__ bool cta_item(const Params& p, int k, int& bh, int& q
   return false;
 }
 
-template <int D>
+// kInner: the launch carries a two-level mask (inner 8 x 8 bitmaps); the
+// other launches are compiled without that code path.
+template <int D, bool kInner>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -568,6 +576,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_run = kNegInf, l_run = 0.f;
       for (int jj = 0; jj < list.n; ++jj, ++j) {
         const int u = list.at(jj);
+        // A partial tile of a two-level mask: this row's 128 key bits, one
+        // byte from each of the 16 inner 8 x 8 blocks it crosses, gathered
+        // while S is being computed.
+        const int pb = kInner ? list.bitmap(jj) : -1;
+        uint32_t mw0 = ~0u, mw1 = ~0u, mw2 = ~0u, mw3 = ~0u;
+        if (kInner && pb >= 0) {
+          const uint8_t* rb = reinterpret_cast<const uint8_t*>(
+                                  p.bits + int64_t(pb) * 256 + (r >> 3) * 16) + (r & 7);
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int cb = 0; cb < 16; ++cb) w[cb >> 2] |= uint32_t(rb[cb * 8]) << (8 * (cb & 3));
+          mw0 = w[0]; mw1 = w[1]; mw2 = w[2]; mw3 = w[3];
+        }
         if (ok)
           ok = mbar_wait_warp(&bar.s_full[t], j & 1, p.status,
                               dev_code(kDevTimeout, kKerAttnTc, 30), abort_flag);
@@ -587,6 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < kBN; ++c)
                 if (c >= lim) sr[c] = __float_as_uint(kNegInf);
+            }
+            if (kInner && pb >= 0) {
+#pragma unroll
+              for (int c = 0; c < kBN; ++c) {
+                const uint32_t w = c < 32 ? mw0 : c < 64 ? mw1 : c < 96 ? mw2 : mw3;
+                if (!((w >> (c & 31)) & 1u)) sr[c] = __float_as_uint(kNegInf);
+              }
             }
             float m8[8];
 #pragma unroll
@@ -622,6 +650,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 64; ++c)
                 if (64 * h + c >= lim) sh1[c] = __float_as_uint(kNegInf);
+            }
+            if (kInner && pb >= 0) {
+              const uint32_t wa = h ? mw2 : mw0, wb = h ? mw3 : mw1;
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (!(((c < 32 ? wa : wb) >> (c & 31)) & 1u)) sh1[c] = __float_as_uint(kNegInf);
             }
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
@@ -746,7 +780,7 @@ bool make_map(CUtensorMap* m, const void* base, int D, int S, int BH) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kInner>
 cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, a.q, D, a.Sq, a.B * a.H) || !make_map(&mk, a.k, D, a.Sk, a.B * a.Hkv) ||
@@ -755,7 +789,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
     return cudaErrorInvalidValue;
   }
   constexpr int smem = Layout<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, kInner>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) {
     *why = "shared memory attribute";
@@ -767,6 +801,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.row_ptr = a.row_ptr; p.col_idx = a.col_idx; p.per_head = a.per_head;
+  p.tile_bits = a.tile_bits; p.bits = a.bits;
   p.nqt = a.nqt; p.nkt = a.nkt;
   p.pairs = (a.nqt + 1) / 2;
   p.o = static_cast<__nv_bfloat16*>(a.o);
@@ -780,7 +815,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
   }
   // two items (a heavy and a light query-tile pair of one head) per CTA
   const int64_t grid = int64_t((p.pairs + 1) / 2) * a.B * a.H;
-  attn_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
+  attn_tc_kernel<D, kInner><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -788,8 +823,9 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
 
 cudaError_t launch_attn_tc_bf16(const AttnArgs& a, cudaStream_t s, const char** why) {
   if (a.Sk == 0) return launch_attn_empty(a, 2, s);
-  if (a.d == 128) return launch_d<128>(a, s, why);
-  return launch_d<64>(a, s, why);
+  const bool inner = a.tile_bits != nullptr;
+  if (a.d == 128) return inner ? launch_d<128, true>(a, s, why) : launch_d<128, false>(a, s, why);
+  return inner ? launch_d<64, true>(a, s, why) : launch_d<64, false>(a, s, why);
 }
 
 }  // namespace rf

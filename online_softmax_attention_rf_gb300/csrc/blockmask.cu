@@ -9,6 +9,12 @@
 // One CTA: (1) one warp per row counts the present tiles with ballots,
 // (2) the CTA scans the counts into row_ptr, (3) one warp per row writes the
 // column indices in ascending order (ballot + prefix popcount).
+//
+// The two-level form (same page, storage format: outer tiles full or
+// partial, one 64-bit bitmap per 8 x 8 inner block of a partial tile) is
+// built from a dense element mask in three launches: one CTA per outer tile
+// classifies it; one CTA lists the non-empty tiles and numbers the partial
+// ones in list order; one CTA per listed partial tile writes its 256 words.
 #include "rf_device.cuh"
 
 namespace rf {
@@ -86,7 +92,184 @@ __global__ void __launch_bounds__(kThreads) blockmask_build_kernel(
   if (overflow) record_status(status, dev_code(kDevCapacity, kKerBlockmask, 1));
 }
 
+// CTA-wide exclusive scan helper state: inclusive per-warp totals.
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_tot,
+                                                        int32_t* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  int32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  const int32_t excl = x - v + (warp > 0 ? warp_tot[warp - 1] : 0);
+  *total = warp_tot[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
+constexpr int kTile = 128, kInner = 8;
+enum : int32_t { kEmpty = 0, kFull = 1, kPartial = 2 };
+
+// E1: class of outer tile blockIdx.x = (n * nqt + qt) * nkt + kt, into state[].
+__global__ void __launch_bounds__(256) tile_class_kernel(const uint8_t* __restrict__ dense,
+                                                         int Sq, int Sk, int nqt, int nkt,
+                                                         int32_t* __restrict__ state) {
+  __shared__ int n_set, n_in;
+  const int64_t tile = blockIdx.x;
+  const int kt = static_cast<int>(tile % nkt);
+  const int qt = static_cast<int>((tile / nkt) % nqt);
+  const int64_t n = tile / (int64_t(nkt) * nqt);
+  if (threadIdx.x == 0) n_set = n_in = 0;
+  __syncthreads();
+  const int r1 = min(kTile, Sq - qt * kTile), c1 = min(kTile, Sk - kt * kTile);
+  const uint8_t* base = dense + (n * Sq + int64_t(qt) * kTile) * Sk + int64_t(kt) * kTile;
+  int set = 0;
+  for (int e = threadIdx.x; e < r1 * kTile; e += blockDim.x) {
+    const int r = e / kTile, c = e % kTile;
+    if (c < c1) set += base[int64_t(r) * Sk + c] != 0;
+  }
+  atomicAdd(&n_set, set);
+  if (threadIdx.x == 0) n_in = r1 * c1;
+  __syncthreads();
+  if (threadIdx.x == 0)
+    state[tile] = n_set == 0 ? kEmpty : (n_set == n_in ? kFull : kPartial);
+}
+
+// E2 (one CTA): row_ptr and col_idx from the states (still in tile_bits),
+// then tile_bits[n] = the partial tile's number in list order, or -1.
+__global__ void __launch_bounds__(1024) two_level_lists_kernel(
+    int64_t nrows, int nkt, int32_t* __restrict__ row_ptr, int32_t* __restrict__ col_idx,
+    int32_t* __restrict__ tile_bits, int64_t bits_cap, int32_t* n_partial, int* status) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  constexpr int32_t kPartialFlag = 1 << 30;
+  // counts per row of outer tiles
+  for (int64_t r = warp; r < nrows; r += nw) {
+    int cnt = 0;
+    for (int c0 = 0; c0 < nkt; c0 += 32) {
+      const int c = c0 + lane;
+      cnt += __popc(__ballot_sync(0xffffffffu, c < nkt && tile_bits[r * nkt + c] != kEmpty));
+    }
+    if (lane == 0) row_ptr[r + 1] = cnt;
+  }
+  if (threadIdx.x == 0) {
+    row_ptr[0] = 0;
+    carry = 0;
+  }
+  __syncthreads();
+  for (int64_t b0 = 0; b0 < nrows; b0 += blockDim.x) {
+    const int64_t r = b0 + threadIdx.x;
+    int32_t tot;
+    const int32_t v = r < nrows ? row_ptr[r + 1] : 0;
+    const int32_t ex = block_exclusive_scan(v, warp_tot, &tot);
+    if (r < nrows) row_ptr[r + 1] = carry + ex + v;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+  // column indices; the partial flag rides in bit 30 until numbered
+  for (int64_t r = warp; r < nrows; r += nw) {
+    int64_t pos = row_ptr[r];
+    for (int c0 = 0; c0 < nkt; c0 += 32) {
+      const int c = c0 + lane;
+      const int32_t st = c < nkt ? tile_bits[r * nkt + c] : kEmpty;
+      const unsigned bal = __ballot_sync(0xffffffffu, st != kEmpty);
+      if (st != kEmpty)
+        col_idx[pos + __popc(bal & ((1u << lane) - 1u))] = c | (st == kPartial ? kPartialFlag : 0);
+      pos += __popc(bal);
+    }
+  }
+  __syncthreads();  // every state has been read; tile_bits is free
+  const int64_t nnz = row_ptr[nrows];
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int64_t b0 = 0; b0 < nnz; b0 += blockDim.x) {
+    const int64_t i = b0 + threadIdx.x;
+    const int32_t ci = i < nnz ? col_idx[i] : 0;
+    const int32_t flag = (ci & kPartialFlag) ? 1 : 0;
+    int32_t tot;
+    const int32_t ex = block_exclusive_scan(flag, warp_tot, &tot);
+    if (i < nnz) {
+      tile_bits[i] = flag ? carry + ex : -1;
+      col_idx[i] = ci & ~kPartialFlag;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (n_partial != nullptr) *n_partial = carry;
+    if (carry > bits_cap) record_status(status, dev_code(kDevCapacity, kKerBlockmask, 2));
+  }
+}
+
+// E3: the 256 words of listed entry blockIdx.x, if it is a partial tile.
+__global__ void __launch_bounds__(256) tile_bits_kernel(const uint8_t* __restrict__ dense,
+                                                        int Sq, int Sk, int nqt, int64_t nrows,
+                                                        const int32_t* __restrict__ row_ptr,
+                                                        const int32_t* __restrict__ col_idx,
+                                                        const int32_t* __restrict__ tile_bits,
+                                                        uint64_t* __restrict__ bits,
+                                                        int64_t bits_cap) {
+  const int64_t i = blockIdx.x;
+  if (i >= row_ptr[nrows]) return;
+  const int32_t p = tile_bits[i];
+  if (p < 0 || p >= bits_cap) return;
+  // the row of outer tiles holding entry i: last r with row_ptr[r] <= i
+  int64_t lo = 0, hi = nrows - 1;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (row_ptr[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  const int64_t n = lo / nqt;
+  const int qt = static_cast<int>(lo % nqt), kt = col_idx[i];
+  const int br = threadIdx.x / (kTile / kInner), bc = threadIdx.x % (kTile / kInner);
+  uint64_t w = 0;
+  for (int r = 0; r < kInner; ++r) {
+    const int row = qt * kTile + br * kInner + r;
+    if (row >= Sq) break;
+    const uint8_t* src = dense + (n * Sq + row) * Sk;
+    for (int c = 0; c < kInner; ++c) {
+      const int col = kt * kTile + bc * kInner + c;
+      if (col < Sk && src[col] != 0) w |= uint64_t(1) << (r * kInner + c);
+    }
+  }
+  bits[int64_t(p) * 256 + threadIdx.x] = w;
+}
+
 }  // namespace
+
+cudaError_t launch_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, int Sk,
+                                            int32_t* row_ptr, int32_t* col_idx,
+                                            int32_t* tile_bits, uint64_t* bits, int64_t bits_cap,
+                                            int32_t* n_partial, cudaStream_t s, int* status) {
+  const int nqt = (Sq + kTile - 1) / kTile, nkt = (Sk + kTile - 1) / kTile;
+  const int64_t ntiles = int64_t(nheads) * nqt * nkt, nrows = int64_t(nheads) * nqt;
+  tile_class_kernel<<<static_cast<unsigned>(ntiles), 256, 0, s>>>(dense, Sq, Sk, nqt, nkt,
+                                                                   tile_bits);
+  // without bitmaps (bits == nullptr) only the lists and the count are built
+  two_level_lists_kernel<<<1, 1024, 0, s>>>(nrows, nkt, row_ptr, col_idx, tile_bits,
+                                            bits != nullptr ? bits_cap : INT64_MAX, n_partial,
+                                            status);
+  if (bits != nullptr)
+    tile_bits_kernel<<<static_cast<unsigned>(ntiles), 256, 0, s>>>(
+        dense, Sq, Sk, nqt, nrows, row_ptr, col_idx, tile_bits, bits, bits_cap);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
                                    int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,

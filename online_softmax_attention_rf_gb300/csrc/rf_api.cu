@@ -153,6 +153,10 @@ rf_status rf_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
       return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask per_head must be 0/1");
     if (Sq > 0 && Sk > 0 && (bm->row_ptr == nullptr || bm->col_idx == nullptr))
       return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask lists are NULL");
+    if (bm->tile_bits != nullptr && bm->bits == nullptr)
+      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask tile_bits without bits");
+    if (bm->bits != nullptr && !aligned(bm->bits, 8))
+      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask bits must be 8-byte aligned");
   }
   if (Sq == 0) return ok();
   if (q == nullptr || o == nullptr || (Sk > 0 && (k == nullptr || v == nullptr)))
@@ -175,6 +179,8 @@ rf_status rf_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
   a.row_ptr = bm ? bm->row_ptr : nullptr;
   a.col_idx = bm ? bm->col_idx : nullptr;
   a.per_head = bm ? bm->per_head : 0;
+  a.tile_bits = bm ? bm->tile_bits : nullptr;
+  a.bits = bm && bm->tile_bits ? bm->bits : nullptr;
   a.nqt = nqt; a.nkt = nkt;
   a.visited = visited;
   a.status = st;
@@ -271,6 +277,29 @@ rf_status rf_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
   cudaError_t e = rf::launch_blockmask_build(dense, nheads, nqt, nkt, row_ptr, col_idx, col_cap,
                                              reinterpret_cast<cudaStream_t>(stream), st);
   if (e != cudaSuccess) return cuda_fail(e, "rf_blockmask_build: launch");
+  return ok();
+}
+
+rf_status rf_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, int Sk,
+                                      int32_t* row_ptr, int32_t* col_idx, int32_t* tile_bits,
+                                      uint64_t* bits, int64_t bits_cap, int32_t* n_partial,
+                                      rf_stream stream) {
+  if (nheads < 1 || Sq < 1 || Sk < 1 || bits_cap < 0)
+    return fail(RF_ERR_INVALID, "rf_blockmask_build_elements: bad sizes");
+  const int64_t ntiles = int64_t(nheads) * cdiv(Sq, 128) * cdiv(Sk, 128);
+  if (ntiles > INT32_MAX / 2)
+    return fail(RF_ERR_INVALID, "rf_blockmask_build_elements: more than 2^30 tiles");
+  if (dense == nullptr || row_ptr == nullptr || col_idx == nullptr || tile_bits == nullptr)
+    return fail(RF_ERR_INVALID, "rf_blockmask_build_elements: NULL pointer");
+  if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(tile_bits, 4) ||
+      (bits != nullptr && !aligned(bits, 8)) || (n_partial != nullptr && !aligned(n_partial, 4)))
+    return fail(RF_ERR_INVALID, "rf_blockmask_build_elements: misaligned output");
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_blockmask_build_elements: no CUDA device");
+  cudaError_t e = rf::launch_blockmask_build_elements(dense, nheads, Sq, Sk, row_ptr, col_idx,
+                                                      tile_bits, bits, bits_cap, n_partial,
+                                                      reinterpret_cast<cudaStream_t>(stream), st);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_blockmask_build_elements: launch");
   return ok();
 }
 

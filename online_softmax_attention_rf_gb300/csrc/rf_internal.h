@@ -53,6 +53,9 @@ struct AttnArgs {
   const int32_t* row_ptr;
   const int32_t* col_idx;
   int per_head;
+  // inner level of the two-level mask (tile_bits == nullptr: all tiles full)
+  const int32_t* tile_bits;
+  const uint64_t* bits;
   int nqt, nkt;
   uint8_t* visited;  // optional debug output, [B*H*nqt*nkt]
   int* status;
@@ -73,5 +76,9 @@ cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void
 cudaError_t launch_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
                                    int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
                                    cudaStream_t s, int* status);
+cudaError_t launch_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, int Sk,
+                                            int32_t* row_ptr, int32_t* col_idx,
+                                            int32_t* tile_bits, uint64_t* bits, int64_t bits_cap,
+                                            int32_t* n_partial, cudaStream_t s, int* status);
 
 }  // namespace rf

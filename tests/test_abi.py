@@ -173,3 +173,17 @@ def test_attn_fwd_host_workspace_size(L):
     dict(ws=None), dict(ws=0x20008), dict(ws_bytes=1024)])
 def test_attn_fwd_host_rejects(L, kw):
     assert _attn_host(L, **kw) == api.RF_ERR_INVALID
+
+
+def test_two_level_validation(L):
+    """Two-level masks: the builder and rf_attn_fwd reject bad arguments on
+    the host (no device memory is touched)."""
+    b = L.rf_blockmask_build_elements
+    assert b(A, 0, 10, 10, A, A, A, A, 4, None, None) == api.RF_ERR_INVALID      # nheads
+    assert b(A, 1, 0, 10, A, A, A, A, 4, None, None) == api.RF_ERR_INVALID      # Sq
+    assert b(None, 1, 10, 10, A, A, A, A, 4, None, None) == api.RF_ERR_INVALID  # dense
+    assert b(A, 1, 10, 10, A, A, None, A, 4, None, None) == api.RF_ERR_INVALID  # tile_bits
+    assert b(A, 1, 10, 10, A, A, A, A + 4, 4, None, None) == api.RF_ERR_INVALID  # bits align
+    assert b(A, 1, 10, 10, A, A, A, A, -1, None, None) == api.RF_ERR_INVALID    # bits_cap
+    bm = api.RFBlockMask(128, 128, 2, 2, A, A, 0, A, None)                      # bits missing
+    assert _attn(L, bm=ctypes.byref(bm)) == api.RF_ERR_INVALID
