@@ -282,9 +282,10 @@ def run_ours(args, dist, rank, world, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
-    if args.only in ("decode", "softmax"):
+    if args.only in ("decode", "softmax", "two_level"):
         # one workload alone (used for profiling captures)
-        fn = bench_decode if args.only == "decode" else bench_softmax
+        fn = {"decode": bench_decode, "softmax": bench_softmax,
+              "two_level": bench_two_level}[args.only]
         out = fn(args, dev, stream, peaks, peak_src)
         if rank == 0:
             print(json.dumps(out), flush=True)
@@ -347,6 +348,7 @@ def run_ours(args, dist, rank, world, local):
     decode = bench_decode(args, dev, stream, peaks, peak_src)
     softmax = bench_softmax(args, dev, stream, peaks, peak_src)
     softmax_long = bench_softmax(args, dev, stream, peaks, peak_src, "rows_1m")
+    two_level = bench_two_level(args, dev, stream, peaks, peak_src)
     launches = args.steps
 
     if rank != 0:
@@ -369,6 +371,7 @@ def run_ours(args, dist, rank, world, local):
         "decode": decode,
         "softmax": softmax,
         "softmax_long": softmax_long,
+        "two_level": two_level,
         "cpu_baseline": {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "%d whole heads of the workload (%.1f s, float64 three-pass "
                                    "NumPy oracle)" % (cpu_heads, cpu_dt)},
@@ -413,6 +416,54 @@ def bench_decode(args, dev, stream, peaks, peak_src):
     return out
 
 
+def bench_two_level(args, dev, stream, peaks, peak_src):
+    """Attention under the two-level (element) mask workload; the device
+    encoder of the mask is timed separately (once per mask)."""
+    from online_softmax_attention_rf_gb300 import api
+    w = inputs.WORKLOADS["two_level"]
+    q_h, k_h, v_h, scale, extras = inputs.workload_inputs("two_level")
+    em = extras["elem_mask"]
+    pairs = int(em.sum())
+    flops = 4.0 * w["d"] * pairs * w["B"] * w["H"]
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    bm = api.BlockMask.from_dense_elements(em, device=dev)
+    # the device encoder alone, on the resident dense mask (one launch set)
+    dense = torch.as_tensor(em).to(dev).to(torch.uint8).unsqueeze(0)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    api.blockmask_build_elements(dense, bm.row_ptr, bm.col_idx, bm.tile_bits, bm.bits)
+    t1.record(stream)
+    t1.synchronize()
+    build_ms = t0.elapsed_time(t1)
+    del dense
+    nnz = int(bm.row_ptr[-1].item())
+    n_partial = int((bm.tile_bits[:nnz] >= 0).sum().item())
+
+    def step():
+        api.attn_fwd(q, k, v, scale, False, bm, o, lse)
+
+    # K and V of a head (4 MB) are re-read from L2 by its CTAs; Q, O (268 MB) exceed L2
+    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    ms = statistics.mean(per)
+    assert api.device_status() == 0
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {"workload": "two_level [B=2, H=16, S=16384, d=64, band 256 + 64 global tokens]",
+           "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "visible_pairs_per_head": pairs,
+           "listed_tiles_per_head": nnz, "partial_tiles_per_head": n_partial,
+           "mask_build_ms": build_ms,
+           "mask_build_note": "rf_blockmask_build_elements on the resident 16384 x 16384 uint8 mask",
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                        "peak_source": "%s dense bf16 (burst)" % peak_src,
+                        "note": "algorithmic flops count visible pairs only"}}
+    del q, k, v, o, lse, bm
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_softmax(args, dev, stream, peaks, peak_src, name="rows_64k"):
     from online_softmax_attention_rf_gb300 import api
     sw = inputs.SOFTMAX_WORKLOADS[name]
@@ -445,7 +496,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax", "two_level"],
+                    default="all",
                     help="time one workload alone (for profiling); the default runs all")
     args = ap.parse_args()
     if args.warmup < 3:

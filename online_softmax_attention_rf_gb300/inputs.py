@@ -34,6 +34,11 @@ WORKLOADS = {
     # block-sparse: sliding window of 8 tiles, diagonal, 10% random lower tiles
     "block_sparse": dict(B=2, H=16, Hkv=16, Sq=16384, Sk=16384, d=64, causal=False,
                          dtype="bf16", seed=4, amp=1.0, tile=128, window=8, frac=0.1),
+    # two-level (element) mask, Longformer-like: keys within `band` of the
+    # query row, plus `n_global` global tokens (first keys, seen by every row;
+    # first rows, which see every key)
+    "two_level": dict(B=2, H=16, Hkv=16, Sq=16384, Sk=16384, d=64, causal=False,
+                      dtype="bf16", seed=8, amp=1.0, band=256, n_global=64),
 }
 
 #: Row-softmax shapes (rows, cols): one row fits a CTA; one row spans a cluster.
@@ -90,6 +95,18 @@ def window_random_tile_mask(nqt, window=8, frac=0.1, seed=4):
     return mask
 
 
+def band_global_mask(S, band, n_global, rows=None):
+    """bool [len(rows), S] element mask: |i - j| <= band, or j < n_global, or
+    i < n_global (all rows by default; built in row blocks to bound memory)."""
+    rows = np.arange(S) if rows is None else np.asarray(rows)
+    out = np.zeros((rows.size, S), dtype=bool)
+    j = np.arange(S, dtype=np.int32)[None, :]
+    for r0 in range(0, rows.size, 1024):
+        i = rows[r0:r0 + 1024, None].astype(np.int32)
+        out[r0:r0 + 1024] = (np.abs(i - j) <= band) | (j < n_global) | (i < n_global)
+    return out
+
+
 def random_tile_mask(nqt, nkt, density, seed, nheads=None):
     """bool [nqt, nkt] (or [nheads, nqt, nkt]) with each tile present w.p. density."""
     rng = np.random.default_rng(seed)
@@ -106,4 +123,6 @@ def workload_inputs(name):
     if name == "block_sparse":
         nqt = n_tiles(w["Sq"], w["tile"])
         extras["tile_mask"] = window_random_tile_mask(nqt, w["window"], w["frac"], w["seed"])
+    if name == "two_level":
+        extras["elem_mask"] = band_global_mask(w["Sq"], w["band"], w["n_global"])
     return q, k, v, default_scale(w["d"]), extras

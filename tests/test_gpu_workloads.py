@@ -61,6 +61,26 @@ def test_block_sparse_sampled(cuda_device):
     _check_prefill("block_sparse", [(0, 0), (1, 15)])
 
 
+def test_two_level_sampled(cuda_device):
+    """The element-masked (two-level) workload at full size: encoder on the
+    device, attention, sampled rows of two heads against the oracle."""
+    w = inputs.WORKLOADS["two_level"]
+    q, k, v, scale, extras = inputs.workload_inputs("two_level")
+    em = extras["elem_mask"]
+    bm = api.BlockMask.from_dense_elements(em)
+    o, lse = api.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale, False, bm)
+    assert api.device_status() == 0
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rows = _sample_rows(w["Sq"], w["seed"]) + [w["n_global"] - 1, w["n_global"], 5000]
+    rows = sorted(set(rows))
+    for b, h in [(0, 0), (1, 15)]:
+        o_ref, lse_ref = oracle.attention(f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, h:h + 1]),
+                                          f64(v[b:b + 1, h:h + 1]), scale, False, rows=rows,
+                                          elem_mask=em)
+        assert_close(o[b, h, rows], o_ref[0, 0], TOL_BF16_O, "two_level O (b=%d,h=%d)" % (b, h))
+        assert_close(lse[b, h, rows], lse_ref[0, 0], TOL_BF16_LSE, "two_level LSE (b=%d,h=%d)" % (b, h))
+
+
 def test_decode_splitk_sampled(cuda_device):
     w = inputs.WORKLOADS["decode_splitk"]
     q, k, v, scale, _ = inputs.workload_inputs("decode_splitk")
