@@ -44,10 +44,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch from ncu captures (summarised under profiles/), valid only for the
 # kernel source they were taken on; any change to the source makes it null.
 TRAFFIC = {
-    # attn_tc_kernel<128> on mha_prefill: dram read 404.1 MB + write 113.4 MB
-    # (sources since then differ only by device helpers the kernel does not use)
-    "attn_tc_mha_prefill": {"digest": "6d1502890a710a2a", "bytes": 517469184,
+    # attn_tc_kernel<128, 0> on mha_prefill: dram read 404.2 MB + write 113.1 MB
+    "attn_tc_mha_prefill": {"digest": "8dc32d453b50a32d", "bytes": 517277696,
                             "sources": ("attn_tc.cu", "rf_device.cuh")},
+    # attn_tc_kernel<64, 1> on two_level: dram__bytes.sum.per_second x duration
+    "attn_tc_two_level": {"digest": "8dc32d453b50a32d", "bytes": 350505000,
+                          "sources": ("attn_tc.cu", "rf_device.cuh")},
     # softmax_rows kernels: dram__bytes.sum.per_second x duration
     "softmax_rows_64k": {"digest": "2e0e34e6b5aed013", "bytes": 2089081000,
                          "sources": ("softmax_rows.cu", "rf_device.cuh")},
@@ -456,7 +458,8 @@ def bench_two_level(args, dev, stream, peaks, peak_src):
            "mask_build_ms": build_ms,
            "mask_build_note": "rf_blockmask_build_elements on the resident 16384 x 16384 uint8 mask",
            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
-                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                        "traffic": traffic_for("attn_tc_two_level"),
                         "peak_source": "%s dense bf16 (burst)" % peak_src,
                         "note": "algorithmic flops count visible pairs only"}}
     del q, k, v, o, lse, bm

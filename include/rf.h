@@ -286,6 +286,21 @@ rf_status rf_blockmask_build_elements(const uint8_t *dense, int nheads, int Sq, 
 rf_status rf_debug_set_visited(uint8_t *visited, int64_t visited_len);
 
 /*
+ * Test aid (fault injection without a GPU fault): every later call on this
+ * host thread that reaches the named site skips one step there, so that a
+ * bounded device wait runs out. 0 turns it off.
+ *  site 1: rf_softmax_rows, a row that one CTA holds on chip (cols * element
+ *          size <= 64 KB, 16-byte aligned): CTA 0 arms the barrier of its
+ *          first shared-memory copy but never issues the copy. Its waits give
+ *          up after the device wait limit (2 s), it records a timeout in the
+ *          device status word (rf_device_status then returns RF_ERR_TIMEOUT),
+ *          waits (bounded) for its own copies in flight and exits; the other
+ *          CTAs and later calls are unaffected.
+ * Errors: RF_ERR_INVALID for an unknown site.
+ */
+rf_status rf_debug_inject_fault(int site);
+
+/*
  * Synchronises the stream, then reads and clears the device status word of
  * the current device. *code receives the raw code (0 = nothing recorded).
  * Returns RF_OK, RF_ERR_TIMEOUT (a wait gave up), RF_ERR_INVALID (a malformed

@@ -61,6 +61,7 @@ SIGNATURES = {
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
     "rf_blockmask_build_elements": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
     "rf_debug_set_visited": (_I, [_P, _I64]),
+    "rf_debug_inject_fault": (_I, [_I]),
     "rf_device_status": (_I, [_P, ctypes.POINTER(_I)]),
     "rf_last_error": (ctypes.c_char_p, []),
     "rf_version": (_I, []),
@@ -323,6 +324,12 @@ def set_debug_visited(buf):
     else:
         _cuda(buf)
         _check(lib().rf_debug_set_visited(_ptr(buf), buf.numel()))
+
+
+def inject_fault(site):
+    """Test aid: later calls on this thread skip one step at ``site`` so that
+    a bounded device wait runs out (rf_debug_inject_fault); 0 turns it off."""
+    _check(lib().rf_debug_inject_fault(int(site)))
 
 
 def device_status():

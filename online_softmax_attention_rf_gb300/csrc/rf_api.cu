@@ -17,6 +17,7 @@ namespace {
 thread_local char g_err[512] = {0};
 thread_local uint8_t* g_visited = nullptr;
 thread_local int64_t g_visited_len = 0;
+thread_local int g_fault_site = 0;
 
 // The device status word (one per device that loads the library).
 __device__ int g_status_word = 0;
@@ -83,6 +84,12 @@ rf_status rf_debug_set_visited(uint8_t* visited, int64_t visited_len) {
   return ok();
 }
 
+rf_status rf_debug_inject_fault(int site) {
+  if (site != 0 && site != 1) return fail(RF_ERR_INVALID, "rf_debug_inject_fault: unknown site");
+  g_fault_site = site;
+  return ok();
+}
+
 rf_status rf_device_status(rf_stream stream, int* code) {
   if (code == nullptr) return fail(RF_ERR_INVALID, "rf_device_status: code is NULL");
   *code = 0;
@@ -116,7 +123,8 @@ rf_status rf_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols, rf
   int* st = rf::status_word();
   if (st == nullptr) return fail(RF_ERR_CUDA, "rf_softmax_rows: no CUDA device");
   cudaError_t e = rf::launch_softmax_rows(x, y, rows, cols, dt,
-                                          reinterpret_cast<cudaStream_t>(stream), st);
+                                          reinterpret_cast<cudaStream_t>(stream), st,
+                                          g_fault_site == 1);
   if (e != cudaSuccess) return cuda_fail(e, "rf_softmax_rows: launch");
   return ok();
 }

@@ -63,8 +63,10 @@ struct AttnArgs {
 
 // Each launcher validates nothing (the entry points do) and returns the
 // launch error, if any.
+// skip_first_copy: fault injection (rf_debug_inject_fault site 1).
 cudaError_t launch_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
-                                rf_dtype dt, cudaStream_t s, int* status);
+                                rf_dtype dt, cudaStream_t s, int* status,
+                                bool skip_first_copy = false);
 cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attn_tc_bf16(const AttnArgs& a, cudaStream_t s, const char** why);
 cudaError_t launch_decode_partials(const void* q, const void* k, const void* v, float* o_part,

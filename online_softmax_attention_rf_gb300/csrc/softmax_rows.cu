@@ -127,9 +127,11 @@ __device__ __forceinline__ void cluster_combine(float m, float l, float2* pairs,
 // Shared-memory-resident row. Row blockIdx is staged in dynamic shared
 // memory as T; float input keeps the probabilities in place, bf16 input keeps
 // x and recomputes the exp.
+// fault != 0 (test aid): CTA 0 arms its first piece's barrier but never
+// issues that copy, so its waits run out and it unwinds.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y, int64_t cols,
-                                                                int bulk, int* status) {
+                                                                int bulk, int* status, int fault) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   T* xs = reinterpret_cast<T*>(smem_raw);
   __shared__ float red[32];
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y
         const int64_t e0 = int64_t(i) * kPerPiece;
         const uint32_t bytes = static_cast<uint32_t>(min64(kPerPiece, n - e0) * sizeof(T));
         mbar_arrive_expect_tx(&bars[i], bytes);
-        bulk_load(xs + e0, xr + e0, bytes, &bars[i], pol);
+        if (!(fault && blockIdx.x == 0 && i == 0)) bulk_load(xs + e0, xr + e0, bytes, &bars[i], pol);
       }
     }
   } else {
@@ -192,7 +194,8 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_onchip(const T* x, T* y
     // never leave with copies in flight
     if (bulk && threadIdx.x == 0)
       for (int i = 0; i < npieces; ++i)
-        mbar_wait(&bars[i], 0, status, dev_code(kDevTimeout, kKerSoftmax, 2), nullptr);
+        if (!(fault && blockIdx.x == 0 && i == 0))  // the copy that was never issued
+          mbar_wait(&bars[i], 0, status, dev_code(kDevTimeout, kKerSoftmax, 2), nullptr);
     return;
   }
   // ---- y = p * scale, 16-byte stores where the slice allows
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y
 
 template <typename T>
 cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStream_t s,
-                         int* status) {
+                         int* status, bool fault) {
   constexpr int64_t cap = kSliceBytes / sizeof(T);  // elements per CTA
   constexpr int64_t vec = 16 / sizeof(T);
   // bulk copies and vector loads need 16-byte aligned rows of whole vectors
@@ -368,7 +371,7 @@ cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStrea
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSliceBytes);
     if (e != cudaSuccess) return e;
     softmax_rows_onchip<T><<<static_cast<unsigned>(rows), kThreads, smem, s>>>(
-        x, y, cols, aligned ? 1 : 0, status);
+        x, y, cols, aligned ? 1 : 0, status, fault ? 1 : 0);
     return cudaGetLastError();
   }
   // one cluster per row, about one slice per CTA
@@ -406,13 +409,14 @@ cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStrea
 }  // namespace
 
 cudaError_t launch_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols, rf_dtype dt,
-                                cudaStream_t s, int* status) {
+                                cudaStream_t s, int* status, bool skip_first_copy) {
   if (rows * kMaxCluster > 0x7fffffffLL) return cudaErrorInvalidValue;  // grid size
   if (dt == RF_F32)
     return launch_typed<float>(static_cast<const float*>(x), static_cast<float*>(y), rows, cols,
-                               s, status);
+                               s, status, skip_first_copy);
   return launch_typed<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x),
-                                     static_cast<__nv_bfloat16*>(y), rows, cols, s, status);
+                                     static_cast<__nv_bfloat16*>(y), rows, cols, s, status,
+                                     skip_first_copy);
 }
 
 }  // namespace rf

@@ -187,3 +187,9 @@ def test_two_level_validation(L):
     assert b(A, 1, 10, 10, A, A, A, A, -1, None, None) == api.RF_ERR_INVALID    # bits_cap
     bm = api.RFBlockMask(128, 128, 2, 2, A, A, 0, A, None)                      # bits missing
     assert _attn(L, bm=ctypes.byref(bm)) == api.RF_ERR_INVALID
+
+
+def test_fault_injection_sites(L):
+    assert L.rf_debug_inject_fault(7) == api.RF_ERR_INVALID
+    assert L.rf_debug_inject_fault(1) == api.RF_OK
+    assert L.rf_debug_inject_fault(0) == api.RF_OK
