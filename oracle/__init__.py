@@ -20,7 +20,11 @@ Modules
                  mask.
 ``incremental``  an independent float64 run of the incremental (online) form,
                  used only to check that the derivation the GPU follows
-                 reaches the three-pass result.
+                 reaches the three-pass result; the same for the pairwise
+                 merge of (count, mean, M2) moment states.
+``cascades``     other cascaded reductions the pages name: top-k softmax
+                 routing of Mixture-of-Experts tokens, and per-row mean and
+                 variance (normalisation statistics).
 
 Every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` against brute force, closed forms, invariants
@@ -40,4 +44,5 @@ from .three_pass import (  # noqa: F401
     visible_mask,
     visited_tiles,
 )
-from .incremental import incremental_attention  # noqa: F401
+from .incremental import incremental_attention, moments_merge, moments_state  # noqa: F401
+from .cascades import moe_route, row_moments  # noqa: F401

@@ -93,3 +93,31 @@ def incremental_attention(q, k, v, scale, vis, tile):
         s = np.where(vis[:, j0:j1], s, NEG_INF)
         state = update(state, s, v[j0:j1])
     return finish(state)
+
+
+# ---------------------------------------------------------------- moments
+# The mean -> centred-sum-of-squares cascade in incremental form: a chunk's
+# state is (n, mean, M2) with M2 = sum (x - mean)^2; two states merge as
+#   n = na + nb, delta = mean_b - mean_a, mean = mean_a + delta * nb / n,
+#   M2 = M2_a + M2_b + delta^2 * na * nb / n
+# (the pairwise update of Chan, Golub and LeVeque), and var = M2 / n. This is
+# the multi-segment form the GPU uses; it is checked against the two-pass
+# definition in row_moments.
+
+def moments_state(x):
+    x = np.asarray(x, dtype=np.float64)
+    n = x.size
+    if n == 0:
+        return (0, 0.0, 0.0)
+    mean = x.sum() / n
+    return (n, mean, float(((x - mean) ** 2).sum()))
+
+
+def moments_merge(a, b):
+    na, ma, qa = a
+    nb, mb, qb = b
+    n = na + nb
+    if n == 0:
+        return (0, 0.0, 0.0)
+    delta = mb - ma
+    return (n, ma + delta * nb / n, qa + qb + delta * delta * na * nb / n)

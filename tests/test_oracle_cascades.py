@@ -1,0 +1,162 @@
+"""Pins of the oracle's other cascaded reductions (``oracle/cascades.py``,
+``oracle/incremental.py`` moment states): brute force with explicit loops,
+library routines (torch.topk / softmax, numpy var), closed forms, invariants,
+and planted mistakes that a pin must catch."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.cascades as oc
+
+
+def _brute_route(row, k, renorm):
+    E = len(row)
+    m = max(row)
+    e = [math.exp(v - m) for v in row]
+    s = math.fsum(e)
+    left = list(range(E))
+    idx = []
+    for _ in range(k):
+        best = left[0]
+        for j in left[1:]:
+            if row[j] > row[best]:            # strict: the lower index wins ties
+                best = j
+        idx.append(best)
+        left.remove(best)
+    w = [e[j] / s for j in idx]
+    if renorm:
+        tot = math.fsum(w)
+        w = [x / tot for x in w]
+    return idx, w, m + math.log(s)
+
+
+@pytest.mark.parametrize("renorm", [False, True])
+def test_moe_route_brute_force(renorm):
+    rng = np.random.default_rng(1)
+    x = rng.normal(size=(7, 11)) * 3
+    x[2, 4] = x[2, 9] = x[2].max() + 1          # a tie at the top
+    idx, w, lse = oracle.moe_route(x, 4, renorm)
+    for t in range(7):
+        bi, bw, bl = _brute_route(x[t].tolist(), 4, renorm)
+        assert idx[t].tolist() == bi
+        np.testing.assert_allclose(w[t], bw, rtol=1e-13, atol=1e-15)
+        assert abs(lse[t] - bl) < 1e-12
+
+
+def test_moe_route_library():
+    """Distinct logits: torch.topk's indices and torch.softmax's values."""
+    x = torch.randn(50, 64, dtype=torch.float64, generator=torch.Generator().manual_seed(2))
+    idx, w, lse = oracle.moe_route(x.numpy(), 6)
+    tv, ti = torch.topk(x, 6, dim=1, largest=True, sorted=True)
+    assert np.array_equal(idx, ti.numpy())
+    p = torch.softmax(x, dim=1)
+    np.testing.assert_allclose(w, torch.gather(p, 1, ti).numpy(), rtol=1e-13)
+    np.testing.assert_allclose(lse, torch.logsumexp(x, 1).numpy(), rtol=1e-13)
+
+
+def test_moe_route_ties_and_special_cases():
+    x = np.array([[0.0, 1.0, 1.0, 1.0, -2.0]])
+    idx, w, _ = oracle.moe_route(x, 3)
+    assert idx.tolist() == [[1, 2, 3]]                        # equal logits: lower index first
+    idx, w, _ = oracle.moe_route(x, 5)
+    assert sorted(idx[0].tolist()) == list(range(5))           # k = E: a permutation
+    np.testing.assert_allclose(w.sum(), 1.0, rtol=1e-14)
+    u = np.zeros((1, 8))
+    idx, w, lse = oracle.moe_route(u, 2, True)                 # uniform: first two, 1/2 each
+    assert idx.tolist() == [[0, 1]] and np.allclose(w, 0.5) and abs(lse[0] - math.log(8)) < 1e-14
+
+
+def test_moe_route_shift_invariance():
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(20, 32))
+    a = oracle.moe_route(x, 5, False)
+    b = oracle.moe_route(x + 17.25, 5, False)
+    assert np.array_equal(a[0], b[0])
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-12)
+    np.testing.assert_allclose(b[2] - a[2], 17.25, rtol=1e-12)
+
+
+def test_row_moments_library_and_closed_forms():
+    rng = np.random.default_rng(4)
+    x = rng.normal(size=(9, 1000)) * 5 + 3
+    mean, var, y = oracle.row_moments(x, eps=0.0)
+    np.testing.assert_allclose(mean, x.mean(axis=1), rtol=1e-13)
+    np.testing.assert_allclose(var, np.var(x, axis=1), rtol=1e-12)      # population variance
+    np.testing.assert_allclose(y.mean(axis=1), 0.0, atol=1e-12)
+    np.testing.assert_allclose((y * y).mean(axis=1), 1.0, rtol=1e-12)
+    m2, v2, y2 = oracle.row_moments(np.array([[2.0, 6.0], [5.0, 5.0]]), eps=0.0 + 1e-30)
+    assert m2.tolist() == [4.0, 5.0] and v2.tolist() == [4.0, 0.0]     # ((a-b)/2)^2; constant row
+    assert np.all(y2[1] == 0.0)
+
+
+def test_row_moments_shift_and_scale():
+    x = np.random.default_rng(5).normal(size=(3, 257))
+    _, v, _ = oracle.row_moments(x)
+    _, vs, _ = oracle.row_moments(x + 1e3)
+    _, vc, _ = oracle.row_moments(3.0 * x)
+    np.testing.assert_allclose(vs, v, rtol=1e-9)
+    np.testing.assert_allclose(vc, 9.0 * v, rtol=1e-12)
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 128, 1000])
+def test_moment_states_merge_to_the_two_pass_result(chunk):
+    """The pairwise (count, mean, M2) merge the GPU uses reaches the
+    two-pass definition for any chunking, and merges associatively."""
+    x = np.random.default_rng(6).normal(size=3001) * 2 + 10
+    st = (0, 0.0, 0.0)
+    for c0 in range(0, x.size, chunk):
+        st = oracle.moments_merge(st, oracle.moments_state(x[c0:c0 + chunk]))
+    mean, var, _ = oracle.row_moments(x[None])
+    assert st[0] == x.size
+    assert abs(st[1] - mean[0]) < 1e-12 and abs(st[2] / st[0] - var[0]) < 1e-10
+    a, b, c = (oracle.moments_state(p) for p in np.split(x[:3000], 3))
+    l = oracle.moments_merge(oracle.moments_merge(a, b), c)
+    r = oracle.moments_merge(a, oracle.moments_merge(b, c))
+    assert abs(l[1] - r[1]) < 1e-12 and abs(l[2] - r[2]) < 1e-8
+
+
+def _pins():
+    yield lambda: test_moe_route_brute_force(True)
+    yield test_moe_route_ties_and_special_cases
+    yield test_row_moments_library_and_closed_forms
+
+
+def _mutant_route_ties_upward(logits, k, renorm=False):
+    x = np.asarray(logits, dtype=np.float64)
+    flipped = x[:, ::-1]
+    idx, w, lse = _orig_route(flipped, k, renorm)
+    return (x.shape[1] - 1 - idx).astype(np.int32), w, lse
+
+
+def _mutant_route_no_renorm(logits, k, renorm=False):
+    return _orig_route(logits, k, False)
+
+
+def _mutant_sample_variance(x, eps=1e-5):
+    x = np.asarray(x, dtype=np.float64)
+    n = x.shape[1]
+    mean = x.sum(axis=1) / n
+    d = x - mean[:, None]
+    var = (d * d).sum(axis=1) / (n - 1)
+    return mean, var, d / np.sqrt(var + eps)[:, None]
+
+
+_orig_route = oc.moe_route
+
+
+@pytest.mark.parametrize("target,mutant", [
+    ("moe_route", _mutant_route_ties_upward), ("moe_route", _mutant_route_no_renorm),
+    ("row_moments", _mutant_sample_variance)])
+def test_pins_catch_planted_mistakes(monkeypatch, target, mutant):
+    monkeypatch.setattr(oracle, target, mutant)
+    failures = 0
+    for pin in _pins():
+        try:
+            pin()
+        except AssertionError:
+            failures += 1
+    assert failures > 0
