@@ -284,10 +284,11 @@ def run_ours(args, dist, rank, world, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
-    if args.only in ("decode", "softmax", "two_level"):
+    if args.only in ("decode", "softmax", "softmax_long", "two_level", "cascades"):
         # one workload alone (used for profiling captures)
         fn = {"decode": bench_decode, "softmax": bench_softmax,
-              "two_level": bench_two_level}[args.only]
+              "softmax_long": lambda *a: bench_softmax(*a, name="rows_1m"),
+              "two_level": bench_two_level, "cascades": bench_cascades}[args.only]
         out = fn(args, dev, stream, peaks, peak_src)
         if rank == 0:
             print(json.dumps(out), flush=True)
@@ -351,6 +352,7 @@ def run_ours(args, dist, rank, world, local):
     softmax = bench_softmax(args, dev, stream, peaks, peak_src)
     softmax_long = bench_softmax(args, dev, stream, peaks, peak_src, "rows_1m")
     two_level = bench_two_level(args, dev, stream, peaks, peak_src)
+    cascades = bench_cascades(args, dev, stream, peaks, peak_src)
     launches = args.steps
 
     if rank != 0:
@@ -374,6 +376,8 @@ def run_ours(args, dist, rank, world, local):
         "softmax": softmax,
         "softmax_long": softmax_long,
         "two_level": two_level,
+        "moe_route": cascades["moe_route"],
+        "row_moments": cascades["row_moments"],
         "cpu_baseline": {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "%d whole heads of the workload (%.1f s, float64 three-pass "
                                    "NumPy oracle)" % (cpu_heads, cpu_dt)},
@@ -493,13 +497,72 @@ def bench_softmax(args, dev, stream, peaks, peak_src, name="rows_64k"):
     return out
 
 
+def bench_cascades(args, dev, stream, peaks, peak_src):
+    """Other cascaded reductions: MoE top-k routing and row moments (both
+    HBM-bound: each input element is read once, outputs written once)."""
+    from online_softmax_attention_rf_gb300 import api
+    out = {}
+    c = inputs.CASCADE_WORKLOADS["moe_route"]
+    x = inputs.make_logits(c["T"], c["E"], c["seed"], c["dtype"], c["amp"]).to(dev)
+    idx = torch.empty(c["T"], c["k"], dtype=torch.int32, device=dev)
+    w = torch.empty(c["T"], c["k"], dtype=torch.float32, device=dev)
+    lse = torch.empty(c["T"], dtype=torch.float32, device=dev)
+    algo = x.numel() * x.element_size() + idx.numel() * 4 + w.numel() * 4 + lse.numel() * 4
+
+    def step_route():
+        api.lib().rf_moe_route(x.data_ptr(), c["T"], c["E"], c["k"], int(c["renorm"]),
+                               idx.data_ptr(), w.data_ptr(), lse.data_ptr(), api.RF_F32,
+                               api._stream())
+
+    # logits + outputs = 138 MB per step, larger than L2 (129 MB): no flush
+    total, per = time_steps(step_route, side_steps(args), args.warmup, stream, None)
+    ms = statistics.mean(per)
+    assert api.device_status() == 0
+    gbs = algo / (ms * 1e-3) / 1e9
+    out["moe_route"] = {
+        "workload": "moe_route [T=%d, E=%d, top %d, renorm] f32 logits" % (c["T"], c["E"], c["k"]),
+        "value": c["T"] / (ms * 1e-3) / 1e9, "unit": "Gtokens/s", "ms_per_step": ms,
+        "algorithmic_bytes": algo,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for("moe_route"),
+                     "peak_source": "%s HBM copy" % peak_src}}
+    del x, idx, w, lse
+    c = inputs.CASCADE_WORKLOADS["row_moments"]
+    x = inputs.make_moment_rows(c["rows"], c["cols"], c["seed"], c["dtype"], c["amp"],
+                                c["offset"]).to(dev)
+    y = torch.empty_like(x)
+    mean = torch.empty(c["rows"], dtype=torch.float32, device=dev)
+    var = torch.empty_like(mean)
+    algo = 2 * x.numel() * x.element_size() + 2 * mean.numel() * 4
+
+    def step_moments():
+        api.lib().rf_row_moments(x.data_ptr(), c["rows"], c["cols"], c["eps"], mean.data_ptr(),
+                                 var.data_ptr(), y.data_ptr(), api.RF_F32, api._stream())
+
+    # x and y (1 GiB) are far larger than L2: no flush needed
+    total, per = time_steps(step_moments, side_steps(args), args.warmup, stream, None)
+    ms = statistics.mean(per)
+    assert api.device_status() == 0
+    gbs = algo / (ms * 1e-3) / 1e9
+    out["row_moments"] = {
+        "workload": "row_moments [%d x %d] f32, normalised rows written" % (c["rows"], c["cols"]),
+        "value": gbs, "unit": "GB/s", "ms_per_step": ms, "algorithmic_bytes": algo,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for("row_moments"),
+                     "peak_source": "%s HBM copy" % peak_src}}
+    del x, y, mean, var
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax", "two_level"],
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax", "softmax_long",
+                                       "two_level", "cascades"],
                     default="all",
                     help="time one workload alone (for profiling); the default runs all")
     args = ap.parse_args()

@@ -276,6 +276,44 @@ rf_status rf_blockmask_build_elements(const uint8_t *dense, int nheads, int Sq, 
                                       rf_stream stream);
 
 /*
+ * Mixture-of-Experts top-k softmax routing (RedFuser page, section 1: MoE
+ * routing is a cascade of reductions; section 4: one of its workloads).
+ * For each token t: p = softmax(logits[t, :]) over the E experts (maximum,
+ * then sum of exponentials), then the k experts with the largest p in
+ * descending order, ties going to the lower expert index (exp is increasing,
+ * so the selection is taken on the logits themselves, as given).
+ *  logits : [T, E] row-major, dtype dt (RF_F32 or RF_BF16), device.
+ *  idx    : int32 [T, k], device, written (expert indices, descending p).
+ *  w      : float [T, k], device, written: p of the selected experts, or,
+ *           with renorm = 1, p divided by the sum of the k selected p.
+ *  lse    : float [T], device, may be NULL: max + log(sum of exponentials).
+ *  T >= 0 (0: nothing launched), 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ * One warp per token reads the token's logits once. Errors: RF_ERR_INVALID
+ * for NULL pointers, sizes out of range or a bad dtype.
+ */
+rf_status rf_moe_route(const void *logits, int64_t T, int E, int k, int renorm, int32_t *idx,
+                       float *w, float *lse, rf_dtype dt, rf_stream stream);
+
+/*
+ * Per-row moments and normalisation (RedFuser page, section 1:
+ * normalisation layers; the Korean page's variance workload): the mean, then
+ * the population variance sum((x - mean)^2) / n, which needs the mean, and
+ * optionally y = (x - mean) / sqrt(var + eps). The two reductions run in one
+ * read of x: each thread folds its elements into a (count, mean, M2) state
+ * and the states merge pairwise (Chan, Golub and LeVeque), the incremental
+ * form of the two-pass definition.
+ *  x    : [rows, cols] row-major, dtype dt (RF_F32 or RF_BF16), device.
+ *  mean, var : float [rows], device, each may be NULL.
+ *  y    : [rows, cols], dtype dt, device, may be NULL (statistics only);
+ *         may alias x.
+ *  rows >= 0, cols >= 0 (either 0: nothing launched); rows <= 2^31 - 1;
+ *  eps >= 0 and finite. A row is read once more from L2 when y is written.
+ * Errors: RF_ERR_INVALID for NULL x with nonzero sizes, bad dtype or eps.
+ */
+rf_status rf_row_moments(const void *x, int64_t rows, int64_t cols, float eps, float *mean,
+                         float *var, void *y, rf_dtype dt, rf_stream stream);
+
+/*
  * Test aid: when visited is non-NULL, every later rf_attn_fwd on this host
  * thread sets visited[((b*H + h) * nqt + qt) * nkt + kt] = 1 for each
  * 128 x 128 tile (qt, kt) whose scores it computes. The caller zeroes the

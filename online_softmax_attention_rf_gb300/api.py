@@ -60,6 +60,8 @@ SIGNATURES = {
     "rf_splitk_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P]),
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
     "rf_blockmask_build_elements": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
+    "rf_moe_route": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _I, _P]),
+    "rf_row_moments": (_I, [_P, _I64, _I64, _F, _P, _P, _P, _I, _P]),
     "rf_debug_set_visited": (_I, [_P, _I64]),
     "rf_debug_inject_fault": (_I, [_I]),
     "rf_device_status": (_I, [_P, ctypes.POINTER(_I)]),
@@ -207,6 +209,39 @@ def softmax_rows(x, out=None):
     _cuda(y)
     _check(lib().rf_softmax_rows(_ptr(x), _ptr(y), x.shape[0], x.shape[1], _dt(x), _stream()))
     return y
+
+
+def moe_route(logits, k, renorm=False, with_lse=True):
+    """rf_moe_route: logits [T, E] -> (idx int32 [T, k], w float32 [T, k], lse or None)."""
+    _cuda(logits)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    T, E = logits.shape
+    idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    lse = torch.empty(T, dtype=torch.float32, device=logits.device) if with_lse else None
+    _check(lib().rf_moe_route(_ptr(logits), T, E, int(k), 1 if renorm else 0, _ptr(idx), _ptr(w),
+                              _ptr(lse), _dt(logits), _stream()))
+    return idx, w, lse
+
+
+def row_moments(x, eps=1e-5, normalize=True, out=None):
+    """rf_row_moments: x [rows, cols] -> (mean, var, y or None), mean/var float32."""
+    _cuda(x)
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, cols]")
+    rows = x.shape[0]
+    mean = torch.empty(rows, dtype=torch.float32, device=x.device)
+    var = torch.empty(rows, dtype=torch.float32, device=x.device)
+    y = None
+    if normalize:
+        y = torch.empty_like(x) if out is None else out
+        _cuda(y)
+        if y.shape != x.shape or y.dtype != x.dtype:
+            raise ValueError("out must match x")
+    _check(lib().rf_row_moments(_ptr(x), rows, x.shape[1], float(eps), _ptr(mean), _ptr(var),
+                                _ptr(y), _dt(x), _stream()))
+    return mean, var, y
 
 
 def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,

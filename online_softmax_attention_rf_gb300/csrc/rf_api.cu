@@ -311,4 +311,37 @@ rf_status rf_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, 
   return ok();
 }
 
+rf_status rf_moe_route(const void* logits, int64_t T, int E, int k, int renorm, int32_t* idx,
+                       float* w, float* lse, rf_dtype dt, rf_stream stream) {
+  if (T < 0) return fail(RF_ERR_INVALID, "rf_moe_route: negative T");
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_moe_route: bad dtype");
+  if (E < 1 || E > 1024) return fail(RF_ERR_INVALID, "rf_moe_route: need 1 <= E <= 1024");
+  if (k < 1 || k > E || k > 32) return fail(RF_ERR_INVALID, "rf_moe_route: need 1 <= k <= min(E, 32)");
+  if (renorm != 0 && renorm != 1) return fail(RF_ERR_INVALID, "rf_moe_route: renorm must be 0 or 1");
+  if (T == 0) return ok();
+  if (logits == nullptr || idx == nullptr || w == nullptr)
+    return fail(RF_ERR_INVALID, "rf_moe_route: NULL pointer");
+  if (cdiv(T, 8) > INT32_MAX) return fail(RF_ERR_INVALID, "rf_moe_route: T too large");
+  cudaError_t e = rf::launch_moe_route(logits, T, E, k, renorm, idx, w, lse, dt,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_moe_route: launch");
+  return ok();
+}
+
+rf_status rf_row_moments(const void* x, int64_t rows, int64_t cols, float eps, float* mean,
+                         float* var, void* y, rf_dtype dt, rf_stream stream) {
+  if (rows < 0 || cols < 0) return fail(RF_ERR_INVALID, "rf_row_moments: negative size");
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_row_moments: bad dtype");
+  if (!(eps >= 0.f) || !std::isfinite(eps))
+    return fail(RF_ERR_INVALID, "rf_row_moments: eps must be finite and >= 0");
+  if (rows == 0 || cols == 0) return ok();
+  if (x == nullptr) return fail(RF_ERR_INVALID, "rf_row_moments: x is NULL");
+  if (rows > INT32_MAX) return fail(RF_ERR_INVALID, "rf_row_moments: rows > 2^31-1");
+  if (cols > (int64_t(1) << 40)) return fail(RF_ERR_INVALID, "rf_row_moments: cols too large");
+  cudaError_t e = rf::launch_row_moments(x, rows, cols, eps, mean, var, y, dt,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_row_moments: launch");
+  return ok();
+}
+
 }  // extern "C"

@@ -78,6 +78,10 @@ cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void
 cudaError_t launch_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
                                    int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
                                    cudaStream_t s, int* status);
+cudaError_t launch_moe_route(const void* logits, int64_t T, int E, int k, int renorm,
+                             int32_t* idx, float* w, float* lse, rf_dtype dt, cudaStream_t s);
+cudaError_t launch_row_moments(const void* x, int64_t rows, int64_t cols, float eps, float* mean,
+                               float* var, void* y, rf_dtype dt, cudaStream_t s);
 cudaError_t launch_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, int Sk,
                                             int32_t* row_ptr, int32_t* col_idx,
                                             int32_t* tile_bits, uint64_t* bits, int64_t bits_cap,

@@ -47,6 +47,16 @@ SOFTMAX_WORKLOADS = {
     "rows_1m": dict(rows=1024, cols=262144, seed=6),
 }
 
+#: Other cascaded reductions. MoE routing: router logits of a prefill batch
+#: for a 256-expert, top-8 model (float32 logits, N(0, amp^2)). Row moments:
+#: normalisation-layer rows (float32, N(offset, amp^2): a mean far from zero
+#: relative to the spread is the case a one-pass sum of squares gets wrong).
+CASCADE_WORKLOADS = {
+    "moe_route": dict(T=131072, E=256, k=8, renorm=True, dtype="f32", seed=9, amp=2.0),
+    "row_moments": dict(rows=16384, cols=8192, dtype="f32", seed=10, amp=1.0, offset=8.0,
+                        eps=1e-5),
+}
+
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -69,6 +79,21 @@ def make_qkv(B, H, Hkv, Sq, Sk, d, seed, dtype="bf16", amp=1.0, dv=None):
 def make_rows(rows, cols, seed, dtype="f32", amp=1.0):
     g = torch.Generator().manual_seed(seed)
     return (torch.randn(rows, cols, generator=g) * amp).to(TORCH_DTYPES[dtype])
+
+
+def make_logits(T, E, seed, dtype="f32", amp=1.0, ties=False):
+    """Router logits [T, E]; ``ties`` draws small integers so that many are equal."""
+    g = torch.Generator().manual_seed(seed)
+    if ties:
+        x = torch.randint(-3, 4, (T, E), generator=g).to(torch.float32)
+    else:
+        x = torch.randn(T, E, generator=g) * amp
+    return x.to(TORCH_DTYPES[dtype])
+
+
+def make_moment_rows(rows, cols, seed, dtype="f32", amp=1.0, offset=0.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(rows, cols, generator=g) * amp + offset).to(TORCH_DTYPES[dtype])
 
 
 def n_tiles(S, tile=128):

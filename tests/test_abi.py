@@ -193,3 +193,27 @@ def test_fault_injection_sites(L):
     assert L.rf_debug_inject_fault(7) == api.RF_ERR_INVALID
     assert L.rf_debug_inject_fault(1) == api.RF_OK
     assert L.rf_debug_inject_fault(0) == api.RF_OK
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=-1), dict(E=0), dict(E=1025), dict(k=0), dict(k=33, E=64), dict(k=9, E=8),
+    dict(renorm=2), dict(dt=9), dict(logits=None), dict(idx=None), dict(w=None)])
+def test_moe_route_rejects(L, kw):
+    a = dict(logits=A, T=16, E=64, k=8, renorm=0, idx=A, w=A, lse=None, dt=api.RF_BF16)
+    a.update(kw)
+    assert L.rf_moe_route(a["logits"], a["T"], a["E"], a["k"], a["renorm"], a["idx"], a["w"],
+                          a["lse"], a["dt"], None) == api.RF_ERR_INVALID
+
+
+def test_moe_route_and_moments_empty_are_no_ops(L):
+    assert L.rf_moe_route(None, 0, 64, 8, 0, None, None, None, api.RF_F32, None) == api.RF_OK
+    assert L.rf_row_moments(None, 0, 64, 1e-5, None, None, None, api.RF_F32, None) == api.RF_OK
+    assert L.rf_row_moments(None, 4, 0, 1e-5, None, None, None, api.RF_F32, None) == api.RF_OK
+
+
+@pytest.mark.parametrize("rows,cols,eps,x,dt", [
+    (-1, 4, 1e-5, A, api.RF_F32), (4, -1, 1e-5, A, api.RF_F32), (4, 4, -1.0, A, api.RF_F32),
+    (4, 4, float("nan"), A, api.RF_F32), (4, 4, float("inf"), A, api.RF_F32),
+    (4, 4, 1e-5, None, api.RF_F32), (4, 4, 1e-5, A, 9), (2 ** 31, 4, 1e-5, A, api.RF_F32)])
+def test_row_moments_rejects(L, rows, cols, eps, x, dt):
+    assert L.rf_row_moments(x, rows, cols, eps, A, A, None, dt, None) == api.RF_ERR_INVALID
