@@ -50,11 +50,17 @@ TRAFFIC = {
     # attn_tc_kernel<64, 1> on two_level: dram__bytes.sum.per_second x duration
     "attn_tc_two_level": {"digest": "8dc32d453b50a32d", "bytes": 350505000,
                           "sources": ("attn_tc.cu", "rf_device.cuh")},
-    # softmax_rows kernels: dram__bytes.sum.per_second x duration
-    "softmax_rows_64k": {"digest": "2e0e34e6b5aed013", "bytes": 2089081000,
+    # softmax_rows kernels: dram__bytes_read.sum + dram__bytes_write.sum
+    "softmax_rows_64k": {"digest": "78500a3290548dca", "bytes": 2087176704,
                          "sources": ("softmax_rows.cu", "rf_device.cuh")},
-    "softmax_rows_1m": {"digest": "2e0e34e6b5aed013", "bytes": 2089842000,
+    "softmax_rows_1m": {"digest": "78500a3290548dca", "bytes": 2088350208,
                         "sources": ("softmax_rows.cu", "rf_device.cuh")},
+    # moe_route_sorted_kernel<float, 8> and row_moments_smem_kernel<float>:
+    # dram__bytes_read.sum + dram__bytes_write.sum
+    "moe_route": {"digest": "8df86f5d7d516d0f", "bytes": 140411392,
+                  "sources": ("cascades.cu", "rf_device.cuh")},
+    "row_moments": {"digest": "8df86f5d7d516d0f", "bytes": 1016724224,
+                    "sources": ("cascades.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
     # (sources since then differ only by device helpers the kernel does not use)
     "decode_partials_decode_splitk": {"digest": "4c12c369bc05677a", "bytes": 4302000000,

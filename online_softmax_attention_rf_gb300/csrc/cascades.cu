@@ -10,21 +10,25 @@
 // MoE routing (one warp per token): the softmax's maximum and sum of
 // exponentials, then k rounds of arg-max over the logits (top-k of the
 // probabilities are the top-k logits: exp is increasing), ties going to the
-// lower expert index. Each lane keeps its best remaining expert; a round is
-// two single-instruction warp reductions (redux.sync) over order-preserving
-// integer keys of the logits -- the largest key, then the lowest index
-// holding it. With up to eight experts per lane, each lane sorts its slots
-// once (a sorting network) and the winner pops the head of its list; with
-// more, the winning lane rescans its slots. The token's logits are read once.
+// lower expert index. A round is two single-instruction warp reductions
+// (redux.sync) over order-preserving integer keys of the logits -- the
+// largest key, then the lowest index holding it. With up to eight experts
+// per lane, each lane sorts its slots once (a sorting network) and the winner
+// pops the head of its list. With more, each lane keeps its best and
+// second-best remaining experts; the winner moves to its second best and
+// rescans its slots only when it wins again with the second best not yet
+// known (for random logits, under one rescan per token). The token's logits
+// are read once.
 //
 // Row moments (one CTA per row): each thread folds its elements into a
-// (count, mean, M2) state, eight at a time (two passes over eight registers,
-// then the pairwise merge of Chan, Golub and LeVeque), the states merge across
-// the warp and the CTA by the same rule (multi-segment strategy, merge step),
-// and var = M2 / n. With an output, a second pass writes (x - mean) /
-// sqrt(var + eps). Rows of up to 32768 elements stay in registers between the
-// two (x is read once); longer rows are read a second time, from L2, where
-// the first pass left them with an evict-last policy.
+// (count, mean, M2) state, four or eight at a time (two passes over
+// registers, then the pairwise merge of Chan, Golub and LeVeque), the states
+// merge across the warp and the CTA by the same rule (multi-segment
+// strategy, merge step), and var = M2 / n. With an output, a second pass
+// writes (x - mean) / sqrt(var + eps). Rows of up to 64 KB are staged in
+// shared memory, float rows of up to 32768 elements otherwise stay in
+// registers between the two (x is read once); longer rows are read a second
+// time, from L2, where the first pass left them with an evict-last policy.
 #include "rf_device.cuh"
 
 namespace rf {
@@ -48,19 +52,24 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// The lane's best remaining expert: the largest key, the lowest slot on ties
-// (slots are in ascending expert order). No slot left: key 0, slot EPL.
+// The lane's best and second-best remaining experts in the order (larger
+// key first, then lower slot): an ascending scan with strict comparisons.
+// Real experts have keys >= 1; key 0 / slot EPL means none.
 template <int EPL>
-__device__ __forceinline__ void local_best(const uint32_t (&key)[EPL], uint32_t taken,
-                                           uint32_t& bk, int& bs) {
-  bk = 0u;
-  bs = EPL;
+__device__ __forceinline__ void top2(const uint32_t (&key)[EPL], uint32_t taken, uint32_t& k1,
+                                     int& s1, uint32_t& k2, int& s2) {
+  k1 = 0u;
+  k2 = 0u;
+  s1 = EPL;
+  s2 = EPL;
 #pragma unroll
-  for (int i = EPL - 1; i >= 0; --i) {
-    if (!((taken >> i) & 1u) && key[i] >= bk) {
-      bk = key[i];
-      bs = i;
-    }
+  for (int i = 0; i < EPL; ++i) {
+    const uint32_t k = ((taken >> i) & 1u) ? 0u : key[i];
+    const bool gt1 = k > k1, gt2 = k > k2;
+    k2 = gt1 ? k1 : (gt2 ? k : k2);
+    s2 = gt1 ? s1 : (gt2 ? i : s2);
+    k1 = gt1 ? k : k1;
+    s1 = gt1 ? i : s1;
   }
 }
 
@@ -80,7 +89,7 @@ __device__ __forceinline__ void route_store(int lane, int64_t t, int k, int reno
   if (lse_out != nullptr && lane == 0) lse_out[t] = m + logf(s);
 }
 
-// Up to 32 experts per lane: the winning lane of a round rescans its slots.
+// 16 or 32 experts per lane: best and second best, rescans when needed.
 template <typename T, int EPL>
 __global__ void __launch_bounds__(256) moe_route_kernel(const T* __restrict__ logits, int64_t T_,
                                                         int E, int k, int renorm,
@@ -91,23 +100,21 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const T* __restrict__ lo
   const int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T_) return;  // whole warps leave together
   const T* row = logits + t * E;
-  // lane l holds experts l, l + 32, ... (coalesced loads); padding slots are
-  // marked taken so that they are never selected
-  uint32_t key[EPL];
+  // lane l holds experts l, l + 32, ... (coalesced loads); padding gets key 0
   float x[EPL];
-  uint32_t taken = 0u;
+  uint32_t key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     x[i] = e < E ? load_f(row + e) : kNegInf;
-    key[i] = order_key(x[i]);
-    if (e >= E) taken |= 1u << i;
+    key[i] = e < E ? max(order_key(x[i]), 1u) : 0u;
   }
-  uint32_t bk;
-  int bs;
-  local_best<EPL>(key, taken, bk, bs);
-  // reduction 1: the maximum (the first selection round's winner)
-  uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+  uint32_t taken = 0u, k1, k2;
+  int s1, s2;
+  top2<EPL>(key, taken, k1, s1, k2, s2);
+  bool second_known = true;
+  // reduction 1: the maximum (the first round's winning key)
+  uint32_t wk = __reduce_max_sync(0xffffffffu, k1);
   const float m = key_value(wk);
   // reduction 2: sum of exp(x - m) (exp(-inf) = 0 for padding)
   float s = 0.f;
@@ -116,16 +123,26 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const T* __restrict__ lo
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   // reduction 3, k rounds: the largest remaining key, then the lowest expert
-  // index among the lanes holding it
+  // index among the lanes holding it (every remaining key is >= 1, so a lane
+  // with nothing left, head key 0, never matches); the winning lane moves to
+  // its second best, or, if that is not known, rescans its slots
   int ri = 0;
   uint32_t rk = 0u;
   for (int r = 0; r < k; ++r) {
-    if (r > 0) wk = __reduce_max_sync(0xffffffffu, bk);
-    const int cand = (bk == wk && bs < EPL) ? lane + 32 * bs : 0x7fffffff;
-    const int wi = __reduce_min_sync(0xffffffffu, cand);
-    if (wi == lane + 32 * bs) {  // the winning lane drops its best and finds the next
-      taken |= 1u << bs;
-      local_best<EPL>(key, taken, bk, bs);
+    if (r > 0) wk = __reduce_max_sync(0xffffffffu, k1);
+    const int my_e = lane + 32 * s1;
+    const bool mine = k1 == wk;
+    const int wi = __reduce_min_sync(0xffffffffu, mine ? my_e : 0x7fffffff);
+    if (mine && wi == my_e) {
+      taken |= 1u << s1;
+      if (second_known) {
+        k1 = k2;
+        s1 = s2;
+        second_known = false;
+      } else {
+        top2<EPL>(key, taken, k1, s1, k2, s2);
+        second_known = true;
+      }
     }
     if (lane == r) {
       ri = wi;
@@ -370,7 +387,8 @@ __global__ void __launch_bounds__(kMomThreads) row_moments_kernel(const T* __res
   }
 }
 
-// Rows of up to NCH * 8 * kMomThreads elements (vec8 rows only): each thread
+// Rows of up to NCH * 8 * kMomThreads elements (vec8 rows only; used for
+// float rows too long for shared memory, up to 32768 elements): each thread
 // holds its NCH eight-element chunks in registers from the load to the
 // normalised store, so x is read from HBM exactly once.
 template <typename T, int NCH>
@@ -425,22 +443,138 @@ __global__ void __launch_bounds__(kMomThreads) row_moments_regs_kernel(
   }
 }
 
+// 16-byte asynchronous global -> shared copies (completion is a hardware
+// wait on the thread's own copy groups; no spin loop).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n"
+               :: "r"(smem_u32(dst)), "l"(src), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
+// Four or eight values of one 16-byte unit (f32 / bf16).
+__device__ __forceinline__ int unit_vals(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  return 4;
+}
+__device__ __forceinline__ int unit_vals(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+  return 8;
+}
+__device__ __forceinline__ void unit_store(float* p, const float (&v)[8], uint64_t pol) {
+  st_global_policy(reinterpret_cast<uint4*>(p),
+                   make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                              __float_as_uint(v[3])), pol);
+}
+__device__ __forceinline__ void unit_store(__nv_bfloat16* p, const float (&v)[8], uint64_t pol) {
+  store8(p, v, pol);
+}
+
+// (count, mean, M2) of the N = 4 or 8 values of a unit: two passes over
+// registers.
+template <int N>
+__device__ __forceinline__ Moments chunk_n(const float (&v)[8]) {
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; ++j) s += v[j];
+  const float mean = s * (1.f / N);
+  float q = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; ++j) q += (v[j] - mean) * (v[j] - mean);
+  return {float(N), mean, q};
+}
+
+constexpr int kSmemThreads = 256;
+constexpr int kSmemRowBytes = 64 * 1024;
+
+// Rows of up to 64 KB (vec8 rows): the CTA copies its row into shared
+// memory in 16-byte units (unit u by thread u mod 256, so a quarter-warp
+// touches 128 contiguous bytes: no bank conflicts), takes the moments from
+// there and writes the normalised row from there: x is read from HBM once.
+// Small CTAs and no registers held across the copy let about seven rows
+// per SM be in flight.
+template <typename T>
+__global__ void __launch_bounds__(kSmemThreads) row_moments_smem_kernel(
+    const T* __restrict__ x, int64_t cols, float eps, float* __restrict__ mean_out,
+    float* __restrict__ var_out, T* __restrict__ y) {
+  extern __shared__ __align__(16) unsigned char srow[];
+  __shared__ Moments part[kSmemThreads / 32];
+  __shared__ float stats[2];
+  constexpr int kPer = 16 / sizeof(T);
+  const int64_t row = blockIdx.x;
+  const int nunits = static_cast<int>(cols / kPer);
+  const unsigned char* src = reinterpret_cast<const unsigned char*>(x + row * cols);
+  const uint64_t drop = policy_evict_first();
+  for (int u = threadIdx.x; u < nunits; u += kSmemThreads)
+    cp_async16(srow + 16 * u, src + 16 * int64_t(u), drop);
+  cp_async_wait_all();
+  __syncthreads();
+  const T* xs = reinterpret_cast<const T*>(srow);
+  Moments st{0.f, 0.f, 0.f};
+  for (int u = threadIdx.x; u < nunits; u += kSmemThreads) {
+    float v[8];
+    unit_vals(xs + u * kPer, v);
+    st = merge(st, chunk_n<kPer>(v));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) st = shfl_merge(st, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = st;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    Moments w = threadIdx.x < kSmemThreads / 32 ? part[threadIdx.x] : Moments{0.f, 0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w = shfl_merge(w, o);
+    if (threadIdx.x == 0) {
+      const float var = w.n > 0.f ? w.m2 / w.n : 0.f;
+      stats[0] = w.mean;
+      stats[1] = var;
+      if (mean_out != nullptr) mean_out[row] = w.mean;
+      if (var_out != nullptr) var_out[row] = var;
+    }
+  }
+  if (y == nullptr) return;
+  __syncthreads();
+  const float mean = stats[0], inv = rsqrtf(stats[1] + eps);
+  T* yr = y + row * cols;
+  for (int u = threadIdx.x; u < nunits; u += kSmemThreads) {
+    float v[8];
+    unit_vals(xs + u * kPer, v);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) v[j] = (v[j] - mean) * inv;
+    unit_store(yr + int64_t(u) * kPer, v, drop);
+  }
+}
+
 template <typename T>
 cudaError_t launch_moments_t(const T* x, int64_t rows, int64_t cols, float eps, float* mean,
                              float* var, T* y, bool vec8, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>(rows);
   const int64_t per_pass = int64_t(8) * kMomThreads;
   const int64_t nch = (cols + per_pass - 1) / per_pass;
-  if (vec8 && nch <= 1)
-    row_moments_regs_kernel<T, 1><<<grid, kMomThreads, 0, s>>>(x, cols, eps, mean, var, y);
-  else if (vec8 && nch <= 2)
-    row_moments_regs_kernel<T, 2><<<grid, kMomThreads, 0, s>>>(x, cols, eps, mean, var, y);
-  else if (vec8 && nch <= 4)
-    row_moments_regs_kernel<T, 4><<<grid, kMomThreads, 0, s>>>(x, cols, eps, mean, var, y);
-  else if (vec8 && nch <= 8)
+  const int64_t row_bytes = cols * int64_t(sizeof(T));
+  if (vec8 && row_bytes <= kSmemRowBytes) {
+    const int smem = static_cast<int>(row_bytes);
+    if (smem > 46 * 1024) {  // with the kernel's static shared memory, past the 48 KB default
+      cudaError_t e = cudaFuncSetAttribute(row_moments_smem_kernel<T>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemRowBytes);
+      if (e != cudaSuccess) return e;
+    }
+    row_moments_smem_kernel<T><<<grid, kSmemThreads, smem, s>>>(x, cols, eps, mean, var, y);
+  } else if (sizeof(T) == 4 && vec8 && nch <= 8) {
+    // float rows of 64 to 128 KB
     row_moments_regs_kernel<T, 8><<<grid, kMomThreads, 0, s>>>(x, cols, eps, mean, var, y);
-  else
+  } else {
     row_moments_kernel<T><<<grid, kMomThreads, 0, s>>>(x, cols, eps, mean, var, y, vec8 ? 1 : 0);
+  }
   return cudaGetLastError();
 }
 
