@@ -290,11 +290,13 @@ def run_ours(args, dist, rank, world, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
-    if args.only in ("decode", "softmax", "softmax_long", "two_level", "cascades"):
+    if args.only in ("decode", "softmax", "softmax_long", "block_sparse", "two_level",
+                     "cascades"):
         # one workload alone (used for profiling captures)
         fn = {"decode": bench_decode, "softmax": bench_softmax,
               "softmax_long": lambda *a: bench_softmax(*a, name="rows_1m"),
-              "two_level": bench_two_level, "cascades": bench_cascades}[args.only]
+              "block_sparse": bench_block_sparse, "two_level": bench_two_level,
+              "cascades": bench_cascades}[args.only]
         out = fn(args, dev, stream, peaks, peak_src)
         if rank == 0:
             print(json.dumps(out), flush=True)
@@ -357,6 +359,7 @@ def run_ours(args, dist, rank, world, local):
     decode = bench_decode(args, dev, stream, peaks, peak_src)
     softmax = bench_softmax(args, dev, stream, peaks, peak_src)
     softmax_long = bench_softmax(args, dev, stream, peaks, peak_src, "rows_1m")
+    block_sparse = bench_block_sparse(args, dev, stream, peaks, peak_src)
     two_level = bench_two_level(args, dev, stream, peaks, peak_src)
     cascades = bench_cascades(args, dev, stream, peaks, peak_src)
     launches = args.steps
@@ -381,6 +384,7 @@ def run_ours(args, dist, rank, world, local):
         "decode": decode,
         "softmax": softmax,
         "softmax_long": softmax_long,
+        "block_sparse": block_sparse,
         "two_level": two_level,
         "moe_route": cascades["moe_route"],
         "row_moments": cascades["row_moments"],
@@ -424,6 +428,39 @@ def bench_decode(args, dev, stream, peaks, peak_src):
                         "note": "step = partials kernel + merge kernel; traffic is the "
                                 "partials kernel's"}}
     del q, k, v, o, lse, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_block_sparse(args, dev, stream, peaks, peak_src):
+    """Block-sparse attention (d = 64, 128 x 128 tiles: sliding window of 8
+    tiles + 10 % of the other lower tiles, 1722 of 16384 per head)."""
+    from online_softmax_attention_rf_gb300 import api
+    w = inputs.WORKLOADS["block_sparse"]
+    q_h, k_h, v_h, scale, extras = inputs.workload_inputs("block_sparse")
+    tm = extras["tile_mask"]
+    flops = 4.0 * w["d"] * visible_pairs(w, tm) * w["B"] * w["H"]
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    bm = api.BlockMask.from_dense(tm, device=dev)
+
+    def step():
+        api.attn_fwd(q, k, v, scale, w["causal"], bm, o, lse)
+
+    # Q, O (268 MB) exceed L2; K and V of a head (4 MB) are re-read from L2
+    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    ms = statistics.mean(per)
+    assert api.device_status() == 0
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {"workload": "block_sparse [B=2, H=16, S=16384, d=64, 1722 of 16384 tiles per head]",
+           "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "listed_tiles_per_head": int(tm.sum()),
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                        "traffic": traffic_for("attn_tc_block_sparse"),
+                        "peak_source": "%s dense bf16 (burst)" % peak_src,
+                        "note": "algorithmic flops count the listed tiles' pairs (non-causal)"}}
+    del q, k, v, o, lse, bm
     torch.cuda.empty_cache()
     return out
 
@@ -568,7 +605,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax", "softmax_long",
-                                       "two_level", "cascades"],
+                                       "block_sparse", "two_level", "cascades"],
                     default="all",
                     help="time one workload alone (for profiling); the default runs all")
     args = ap.parse_args()
