@@ -291,12 +291,12 @@ def run_ours(args, dist, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
     if args.only in ("decode", "softmax", "softmax_long", "block_sparse", "two_level",
-                     "cascades"):
+                     "scattered", "cascades"):
         # one workload alone (used for profiling captures)
         fn = {"decode": bench_decode, "softmax": bench_softmax,
               "softmax_long": lambda *a: bench_softmax(*a, name="rows_1m"),
               "block_sparse": bench_block_sparse, "two_level": bench_two_level,
-              "cascades": bench_cascades}[args.only]
+              "scattered": bench_scattered, "cascades": bench_cascades}[args.only]
         out = fn(args, dev, stream, peaks, peak_src)
         if rank == 0:
             print(json.dumps(out), flush=True)
@@ -361,6 +361,7 @@ def run_ours(args, dist, rank, world, local):
     softmax_long = bench_softmax(args, dev, stream, peaks, peak_src, "rows_1m")
     block_sparse = bench_block_sparse(args, dev, stream, peaks, peak_src)
     two_level = bench_two_level(args, dev, stream, peaks, peak_src)
+    scattered = bench_scattered(args, dev, stream, peaks, peak_src)
     cascades = bench_cascades(args, dev, stream, peaks, peak_src)
     launches = args.steps
 
@@ -386,6 +387,7 @@ def run_ours(args, dist, rank, world, local):
         "softmax_long": softmax_long,
         "block_sparse": block_sparse,
         "two_level": two_level,
+        "scattered_short": scattered,
         "moe_route": cascades["moe_route"],
         "row_moments": cascades["row_moments"],
         "cpu_baseline": {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -460,6 +462,49 @@ def bench_block_sparse(args, dev, stream, peaks, peak_src):
                         "traffic": traffic_for("attn_tc_block_sparse"),
                         "peak_source": "%s dense bf16 (burst)" % peak_src,
                         "note": "algorithmic flops count the listed tiles' pairs (non-causal)"}}
+    del q, k, v, o, lse, bm
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_scattered(args, dev, stream, peaks, peak_src):
+    """Short sequences under a scattered element mask (STOF's row-wise
+    kernel regime): both kernels timed, and the analytic selector's choice."""
+    from online_softmax_attention_rf_gb300 import api
+    w = inputs.WORKLOADS["scattered_short"]
+    q_h, k_h, v_h, scale, extras = inputs.workload_inputs("scattered_short")
+    em = extras["elem_mask"]
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    bm = api.BlockMask.from_dense_elements(em, device=dev)
+    counts = api.selector_counts(w["B"], w["H"], w["Sq"], w["Sk"], False, bm)
+    choice = api.choose_kernel(w["B"], w["H"], w["Sq"], w["Sk"], w["d"], *counts, device=dev)
+    est_block, est_row = api.estimate_us(w["B"], w["H"], w["Sq"], w["Sk"], w["d"], *counts,
+                                         device=dev)
+    flops = 4.0 * w["d"] * counts[2]
+    times = {}
+    for kern in ("block", "row"):
+        def step(kern=kern):
+            api.attn_fwd(q, k, v, scale, False, bm, o, lse, kernel=kern)
+
+        # Q, K, V, O are 134 MB (above L2); K and V of a head (256 KB) are re-read
+        _, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+        times[kern] = statistics.mean(per)
+    assert api.device_status() == 0
+    chosen = "row" if choice == api.RF_KERNEL_ROWWISE else "block"
+    ms = times[chosen]
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {"workload": "scattered_short [B=16, H=16, S=1024, d=64; window 16, 8 global, "
+                       "1 % random keys]",
+           "value": tf, "unit": "TFLOP/s (visible pairs)", "ms_per_step": ms,
+           "selected_kernel": chosen, "ms_block": times["block"], "ms_row": times["row"],
+           "model_us": {"block": est_block, "row": est_row},
+           "listed_tiles": counts[0], "partial_tiles": counts[1], "visible_pairs": counts[2],
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                        "traffic": None, "peak_source": "%s dense bf16 (burst)" % peak_src,
+                        "note": "flops over visible pairs only"}}
     del q, k, v, o, lse, bm
     torch.cuda.empty_cache()
     return out
@@ -605,7 +650,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax", "softmax_long",
-                                       "block_sparse", "two_level", "cascades"],
+                                       "block_sparse", "two_level", "scattered", "cascades"],
                     default="all",
                     help="time one workload alone (for profiling); the default runs all")
     args = ap.parse_args()

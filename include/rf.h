@@ -276,6 +276,47 @@ rf_status rf_blockmask_build_elements(const uint8_t *dense, int nheads, int Sq, 
                                       rf_stream stream);
 
 /*
+ * Row-wise attention: the same operation and arguments as rf_attn_fwd, by
+ * STOF's row-wise kernel (Accelerating Sparse Transformer Inference on GPU,
+ * Méthodologie, unified MHA module, dual-kernel strategy: Q split into rows,
+ * warp-level shuffles, no synchronisation between warps). One warp per query
+ * row visits only the row's visible keys -- all keys of a full listed tile,
+ * the set bits of a partial tile's inner bitmaps, up to the causal limit --
+ * in float32 (bf16 inputs widened exactly; P is not rounded), so its work is
+ * proportional to the visible pairs rather than to the listed tiles. For
+ * highly sparse masks on short sequences. d must be 64 or 128 (f32 or bf16).
+ * The rf_debug_set_visited test aid does not apply to this kernel.
+ * Errors: those of rf_attn_fwd; RF_ERR_UNSUPPORTED for d outside {64, 128}.
+ */
+rf_status rf_attn_fwd_rowwise(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int H, int Hkv, int Sq, int Sk, int d, float scale,
+                              int causal, const rf_blockmask *blockmask, rf_dtype dt,
+                              rf_stream stream);
+
+#define RF_KERNEL_BLOCKWISE 0  /* rf_attn_fwd */
+#define RF_KERNEL_ROWWISE 1    /* rf_attn_fwd_rowwise */
+
+/*
+ * STOF's kernel selection (same page, unified MHA module): an analytic model
+ * of both kernels' times from the mask's sparsity and the sequence length.
+ *  listed_tiles : 128 x 128 tiles listed over all B*H heads (a shared mask
+ *                 counts once per head); partial_tiles: how many of them are
+ *                 partial (two-level masks), 0 <= partial <= listed;
+ *  visible_pairs: visible (query, key) pairs over all heads (after causal);
+ *  num_sms      : streaming multiprocessors of the device (152 on GB300).
+ * rf_attn_choose_kernel returns RF_KERNEL_BLOCKWISE or RF_KERNEL_ROWWISE
+ * (the smaller estimate), or -1 for invalid arguments (B, H, Sq >= 1,
+ * Sk >= 0, d in {64, 128}, counts >= 0, num_sms >= 1). rf_attn_estimate_us
+ * writes both estimates in microseconds (RF_ERR_INVALID on bad arguments or
+ * NULL outputs). Pure host functions: no CUDA call.
+ */
+int rf_attn_choose_kernel(int B, int H, int Sq, int Sk, int d, int64_t listed_tiles,
+                          int64_t partial_tiles, int64_t visible_pairs, int num_sms);
+int rf_attn_estimate_us(int B, int H, int Sq, int Sk, int d, int64_t listed_tiles,
+                        int64_t partial_tiles, int64_t visible_pairs, int num_sms,
+                        double *block_us, double *row_us);
+
+/*
  * Mixture-of-Experts top-k softmax routing (RedFuser page, section 1: MoE
  * routing is a cascade of reductions; section 4: one of its workloads).
  * For each token t: p = softmax(logits[t, :]) over the E experts (maximum,

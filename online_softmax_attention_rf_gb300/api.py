@@ -12,12 +12,14 @@ import ctypes
 import math
 import os
 
+import numpy as np
 import torch
 
 from . import build as _build
 
 RF_OK, RF_ERR_INVALID, RF_ERR_UNSUPPORTED, RF_ERR_CUDA, RF_ERR_TIMEOUT = range(5)
 RF_F32, RF_BF16 = 0, 1
+RF_KERNEL_BLOCKWISE, RF_KERNEL_ROWWISE = 0, 1
 _STATUS_NAMES = {0: "RF_OK", 1: "RF_ERR_INVALID", 2: "RF_ERR_UNSUPPORTED", 3: "RF_ERR_CUDA",
                  4: "RF_ERR_TIMEOUT"}
 TILE = 128
@@ -60,6 +62,11 @@ SIGNATURES = {
     "rf_splitk_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P]),
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
     "rf_blockmask_build_elements": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
+    "rf_attn_fwd_rowwise": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
+                                 ctypes.POINTER(RFBlockMask), _I, _P]),
+    "rf_attn_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I64, _I64, _I64, _I]),
+    "rf_attn_estimate_us": (_I, [_I, _I, _I, _I, _I, _I64, _I64, _I64, _I,
+                                 ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "rf_moe_route": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _I, _P]),
     "rf_row_moments": (_I, [_P, _I64, _I64, _F, _P, _P, _P, _I, _P]),
     "rf_debug_set_visited": (_I, [_P, _I64]),
@@ -132,10 +139,14 @@ class BlockMask:
     tile) and ``bits`` uint64 viewed as int64 [partial tiles, 256].
     """
 
-    def __init__(self, row_ptr, col_idx, nqt, nkt, per_head, tile_bits=None, bits=None):
+    def __init__(self, row_ptr, col_idx, nqt, nkt, per_head, tile_bits=None, bits=None,
+                 host_mask=None):
         self.row_ptr, self.col_idx = row_ptr, col_idx
         self.nqt, self.nkt, self.per_head = nqt, nkt, per_head
         self.tile_bits, self.bits = tile_bits, bits
+        # host copy of the mask it was built from (tile or element level),
+        # for the kernel selector's counts; None when built from lists
+        self.host_mask = host_mask
 
     def as_struct(self):
         return RFBlockMask(TILE, TILE, self.nqt, self.nkt, self.row_ptr.data_ptr(),
@@ -163,7 +174,8 @@ class BlockMask:
         blockmask_build_elements(dense, row_ptr, col_idx, tile_bits, None, n_partial)
         bits = torch.empty((max(1, int(n_partial.item())), 256), dtype=torch.int64, device=device)
         blockmask_build_elements(dense, row_ptr, col_idx, tile_bits, bits, n_partial)
-        return cls(row_ptr, col_idx, nqt, nkt, per_head, tile_bits, bits)
+        return cls(row_ptr, col_idx, nqt, nkt, per_head, tile_bits, bits,
+                   host_mask=("elements", em.cpu().numpy().astype(bool)))
 
     @classmethod
     def from_dense(cls, tile_mask, device="cuda"):
@@ -178,7 +190,8 @@ class BlockMask:
         row_ptr = torch.empty(nheads * nqt + 1, dtype=torch.int32, device=device)
         col_idx = torch.empty(max(1, nheads * nqt * nkt), dtype=torch.int32, device=device)
         blockmask_build(dense, row_ptr, col_idx)
-        return cls(row_ptr, col_idx, nqt, nkt, per_head)
+        return cls(row_ptr, col_idx, nqt, nkt, per_head,
+                   host_mask=("tiles", tm.cpu().numpy().astype(bool)))
 
 
 def blockmask_build(dense_u8, row_ptr, col_idx):
@@ -245,21 +258,102 @@ def row_moments(x, eps=1e-5, normalize=True, out=None):
 
 
 def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,
-             with_lse=True):
-    """rf_attn_fwd: q [B,H,Sq,d], k/v [B,Hkv,Sk,d] -> (o, lse or None)."""
+             with_lse=True, kernel="block"):
+    """rf_attn_fwd (kernel "block"), rf_attn_fwd_rowwise ("row"), or the one
+    rf_attn_choose_kernel picks ("auto"): q [B,H,Sq,d], k/v [B,Hkv,Sk,d] ->
+    (o, lse or None)."""
     _cuda(q, k, v)
     B, H, Sq, d = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if kernel == "auto":
+        counts = selector_counts(B, H, Sq, Sk, causal, blockmask)
+        kernel = "row" if choose_kernel(B, H, Sq, Sk, d, *counts, device=q.device) == \
+            RF_KERNEL_ROWWISE else "block"
+    if kernel not in ("block", "row"):
+        raise ValueError("kernel must be 'block', 'row' or 'auto'")
     o = torch.empty_like(q) if out is None else out
     if lse is None and with_lse:
         lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
     _cuda(o, lse)
     bm = ctypes.byref(blockmask.as_struct()) if blockmask is not None else None
-    _check(lib().rf_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Sq, Sk, d,
-                             float(scale), 1 if causal else 0, bm, _dt(q), _stream()))
+    fn = lib().rf_attn_fwd if kernel == "block" else lib().rf_attn_fwd_rowwise
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Sq, Sk, d, float(scale),
+              1 if causal else 0, bm, _dt(q), _stream()))
     return o, lse
+
+
+def attn_fwd_rowwise(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,
+                     with_lse=True):
+    """rf_attn_fwd_rowwise (STOF's row-wise kernel); arguments as attn_fwd."""
+    return attn_fwd(q, k, v, scale, causal, blockmask, out, lse, with_lse, kernel="row")
+
+
+def choose_kernel(B, H, Sq, Sk, d, listed_tiles, partial_tiles, visible_pairs, num_sms=None,
+                  device=None):
+    """rf_attn_choose_kernel: RF_KERNEL_BLOCKWISE or RF_KERNEL_ROWWISE."""
+    if num_sms is None:
+        num_sms = _num_sms(device)
+    r = lib().rf_attn_choose_kernel(B, H, Sq, Sk, d, int(listed_tiles), int(partial_tiles),
+                                    int(visible_pairs), int(num_sms))
+    if r < 0:
+        raise ValueError("rf_attn_choose_kernel: invalid arguments")
+    return r
+
+
+def estimate_us(B, H, Sq, Sk, d, listed_tiles, partial_tiles, visible_pairs, num_sms=None,
+                device=None):
+    """rf_attn_estimate_us: (block-wise, row-wise) model times in microseconds."""
+    if num_sms is None:
+        num_sms = _num_sms(device)
+    b, r = ctypes.c_double(), ctypes.c_double()
+    _check(lib().rf_attn_estimate_us(B, H, Sq, Sk, d, int(listed_tiles), int(partial_tiles),
+                                     int(visible_pairs), int(num_sms), ctypes.byref(b),
+                                     ctypes.byref(r)))
+    return b.value, r.value
+
+
+def _num_sms(device):
+    if torch.cuda.is_available():
+        dev = torch.cuda.current_device() if device is None else torch.device(device).index or 0
+        return torch.cuda.get_device_properties(dev).multi_processor_count
+    return 152
+
+
+def selector_counts(B, H, Sq, Sk, causal, blockmask=None):
+    """(listed_tiles, partial_tiles, visible_pairs) over all B*H heads: the
+    selector's inputs, counted on the host from the mask a BlockMask was built
+    from (dense when blockmask is None)."""
+    nqt, nkt = -(-Sq // TILE), -(-Sk // TILE)
+    rows = np.arange(Sq)[:, None]
+    cols = np.arange(Sk)[None, :]
+    vis = (cols <= rows + (Sk - Sq)) if causal else np.ones((Sq, Sk), dtype=bool)
+    heads = B * H
+    kind, m = ("dense", None) if blockmask is None else (blockmask.host_mask or (None, None))
+    if kind is None:
+        raise ValueError("this BlockMask keeps no host mask; pass the counts yourself")
+    if kind == "dense":
+        em = vis[None]
+    elif kind == "tiles":
+        em = np.repeat(np.repeat(m, TILE, axis=-2), TILE, axis=-1)[..., :Sq, :Sk] & vis
+    else:
+        em = m & vis
+
+    def per_tile(x):
+        pad = np.zeros((x.shape[0], nqt * TILE, nkt * TILE), dtype=bool)
+        pad[:, :Sq, :Sk] = x
+        return pad.reshape(x.shape[0], nqt, TILE, nkt, TILE).sum(axis=(2, 4))
+
+    listed = per_tile(em) > 0
+    if kind == "elements":
+        # partial in the two-level encoding (the causal limit costs nothing extra)
+        inside = np.ones((1, Sq, Sk), dtype=bool)
+        partial = listed & (per_tile(m) < per_tile(inside))
+    else:
+        partial = np.zeros_like(listed)
+    scale = heads if em.shape[0] == 1 else 1
+    return (int(listed.sum()) * scale, int(partial.sum()) * scale, int(em.sum()) * scale)
 
 
 def attn_fwd_host_workspace_bytes(B, H, Hkv, Sq, Sk, d, dtype=torch.bfloat16):

@@ -70,6 +70,82 @@ uint8_t* debug_visited(int64_t* len) {
 
 }  // namespace rf
 
+namespace {
+
+// Validation shared by the attention entry points; fills `a`. *empty: Sq is
+// 0 (nothing to launch).
+rf_status attn_prepare(const char* fn, const void* q, const void* k, const void* v, void* o,
+                       float* lse, int B, int H, int Hkv, int Sq, int Sk, int d, float scale,
+                       int causal, const rf_blockmask* bm, rf_dtype dt, rf::AttnArgs& a,
+                       bool* empty) {
+  *empty = false;
+  if (B < 1 || H < 1 || Hkv < 1 || Sq < 0 || Sk < 0 || d < 1)
+    return fail(RF_ERR_INVALID, "%s: bad sizes B=%d H=%d Hkv=%d Sq=%d Sk=%d d=%d", fn, B, H,
+                Hkv, Sq, Sk, d);
+  if (Sq > (1 << 30) || Sk > (1 << 30))
+    return fail(RF_ERR_INVALID, "%s: Sq and Sk must be <= 2^30", fn);
+  if (H % Hkv != 0) return fail(RF_ERR_INVALID, "%s: H %% Hkv != 0", fn);
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(RF_ERR_INVALID, "%s: scale must be finite and > 0", fn);
+  if (causal != 0 && causal != 1) return fail(RF_ERR_INVALID, "%s: causal must be 0/1", fn);
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "%s: bad dtype", fn);
+  if (dt == RF_BF16 && d != 64 && d != 128)
+    return fail(RF_ERR_UNSUPPORTED, "%s: bf16 supports d in {64,128}, got %d", fn, d);
+  if (dt == RF_F32 && (d % 4 != 0 || d > 256))
+    return fail(RF_ERR_UNSUPPORTED, "%s: f32 supports d %% 4 == 0, d <= 256", fn);
+  const int64_t esz = dt == RF_F32 ? 4 : 2;
+  if (int64_t(B) * H * Sq * d * esz > (int64_t(1) << 46) ||
+      int64_t(B) * Hkv * Sk * d * esz > (int64_t(1) << 46))
+    return fail(RF_ERR_INVALID, "%s: tensors too large", fn);
+  const int nqt = static_cast<int>(cdiv(Sq, 128)), nkt = static_cast<int>(cdiv(Sk, 128));
+  if (bm != nullptr) {
+    if (bm->tile_q != 128 || bm->tile_k != 128)
+      return fail(RF_ERR_INVALID, "%s: blockmask tiles must be 128x128", fn);
+    if (bm->nqt != nqt || bm->nkt != nkt)
+      return fail(RF_ERR_INVALID, "%s: blockmask nqt/nkt (%d,%d) != (%d,%d)", fn, bm->nqt,
+                  bm->nkt, nqt, nkt);
+    if (bm->per_head != 0 && bm->per_head != 1)
+      return fail(RF_ERR_INVALID, "%s: blockmask per_head must be 0/1", fn);
+    if (Sq > 0 && Sk > 0 && (bm->row_ptr == nullptr || bm->col_idx == nullptr))
+      return fail(RF_ERR_INVALID, "%s: blockmask lists are NULL", fn);
+    if (bm->tile_bits != nullptr && bm->bits == nullptr)
+      return fail(RF_ERR_INVALID, "%s: blockmask tile_bits without bits", fn);
+    if (bm->bits != nullptr && !aligned(bm->bits, 8))
+      return fail(RF_ERR_INVALID, "%s: blockmask bits must be 8-byte aligned", fn);
+  }
+  if (Sq == 0) {
+    *empty = true;
+    return ok();
+  }
+  if (q == nullptr || o == nullptr || (Sk > 0 && (k == nullptr || v == nullptr)))
+    return fail(RF_ERR_INVALID, "%s: NULL tensor pointer", fn);
+  if (!aligned(q, 16) || !aligned(o, 16) || (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))))
+    return fail(RF_ERR_INVALID, "%s: q/k/v/o must be 16-byte aligned", fn);
+  if (lse != nullptr && !aligned(lse, 4))
+    return fail(RF_ERR_INVALID, "%s: lse must be 4-byte aligned", fn);
+  int64_t vlen = 0;
+  uint8_t* visited = rf::debug_visited(&vlen);
+  if (visited != nullptr && vlen < int64_t(B) * H * nqt * nkt)
+    return fail(RF_ERR_INVALID, "%s: visited buffer too small", fn);
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "%s: no CUDA device", fn);
+
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.Sq = Sq; a.Sk = Sk; a.d = d;
+  a.scale = scale; a.causal = causal;
+  a.row_ptr = bm ? bm->row_ptr : nullptr;
+  a.col_idx = bm ? bm->col_idx : nullptr;
+  a.per_head = bm ? bm->per_head : 0;
+  a.tile_bits = bm ? bm->tile_bits : nullptr;
+  a.bits = bm && bm->tile_bits ? bm->bits : nullptr;
+  a.nqt = nqt; a.nkt = nkt;
+  a.visited = visited;
+  a.status = st;
+  return ok();
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* rf_last_error(void) { return g_err; }
@@ -132,66 +208,11 @@ rf_status rf_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols, rf
 rf_status rf_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int H, int Hkv, int Sq, int Sk, int d, float scale, int causal,
                       const rf_blockmask* bm, rf_dtype dt, rf_stream stream) {
-  if (B < 1 || H < 1 || Hkv < 1 || Sq < 0 || Sk < 0 || d < 1)
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: bad sizes B=%d H=%d Hkv=%d Sq=%d Sk=%d d=%d", B, H,
-                Hkv, Sq, Sk, d);
-  if (Sq > (1 << 30) || Sk > (1 << 30))
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: Sq and Sk must be <= 2^30");
-  if (H % Hkv != 0) return fail(RF_ERR_INVALID, "rf_attn_fwd: H %% Hkv != 0");
-  if (!(scale > 0.f) || !std::isfinite(scale))
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: scale must be finite and > 0");
-  if (causal != 0 && causal != 1) return fail(RF_ERR_INVALID, "rf_attn_fwd: causal must be 0/1");
-  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_attn_fwd: bad dtype");
-  if (dt == RF_BF16 && d != 64 && d != 128)
-    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: bf16 supports d in {64,128}, got %d", d);
-  if (dt == RF_F32 && (d % 4 != 0 || d > 256))
-    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: f32 supports d %% 4 == 0, d <= 256");
-  const int64_t esz = dt == RF_F32 ? 4 : 2;
-  if (int64_t(B) * H * Sq * d * esz > (int64_t(1) << 46) ||
-      int64_t(B) * Hkv * Sk * d * esz > (int64_t(1) << 46))
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: tensors too large");
-  const int nqt = static_cast<int>(cdiv(Sq, 128)), nkt = static_cast<int>(cdiv(Sk, 128));
-  if (bm != nullptr) {
-    if (bm->tile_q != 128 || bm->tile_k != 128)
-      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask tiles must be 128x128");
-    if (bm->nqt != nqt || bm->nkt != nkt)
-      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask nqt/nkt (%d,%d) != (%d,%d)", bm->nqt,
-                  bm->nkt, nqt, nkt);
-    if (bm->per_head != 0 && bm->per_head != 1)
-      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask per_head must be 0/1");
-    if (Sq > 0 && Sk > 0 && (bm->row_ptr == nullptr || bm->col_idx == nullptr))
-      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask lists are NULL");
-    if (bm->tile_bits != nullptr && bm->bits == nullptr)
-      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask tile_bits without bits");
-    if (bm->bits != nullptr && !aligned(bm->bits, 8))
-      return fail(RF_ERR_INVALID, "rf_attn_fwd: blockmask bits must be 8-byte aligned");
-  }
-  if (Sq == 0) return ok();
-  if (q == nullptr || o == nullptr || (Sk > 0 && (k == nullptr || v == nullptr)))
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: NULL tensor pointer");
-  if (!aligned(q, 16) || !aligned(o, 16) || (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))))
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: q/k/v/o must be 16-byte aligned");
-  if (lse != nullptr && !aligned(lse, 4))
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: lse must be 4-byte aligned");
-  int64_t vlen = 0;
-  uint8_t* visited = rf::debug_visited(&vlen);
-  if (visited != nullptr && vlen < int64_t(B) * H * nqt * nkt)
-    return fail(RF_ERR_INVALID, "rf_attn_fwd: visited buffer too small");
-  int* st = rf::status_word();
-  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_attn_fwd: no CUDA device");
-
   rf::AttnArgs a{};
-  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.B = B; a.H = H; a.Hkv = Hkv; a.Sq = Sq; a.Sk = Sk; a.d = d;
-  a.scale = scale; a.causal = causal;
-  a.row_ptr = bm ? bm->row_ptr : nullptr;
-  a.col_idx = bm ? bm->col_idx : nullptr;
-  a.per_head = bm ? bm->per_head : 0;
-  a.tile_bits = bm ? bm->tile_bits : nullptr;
-  a.bits = bm && bm->tile_bits ? bm->bits : nullptr;
-  a.nqt = nqt; a.nkt = nkt;
-  a.visited = visited;
-  a.status = st;
+  bool empty = false;
+  const rf_status pst = attn_prepare("rf_attn_fwd", q, k, v, o, lse, B, H, Hkv, Sq, Sk, d, scale,
+                                     causal, bm, dt, a, &empty);
+  if (pst != RF_OK || empty) return pst;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (dt == RF_F32) {
@@ -203,6 +224,21 @@ rf_status rf_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
       return fail(RF_ERR_CUDA, "rf_attn_fwd: %s: %s", why, cudaGetErrorString(e));
   }
   if (e != cudaSuccess) return cuda_fail(e, "rf_attn_fwd: launch");
+  return ok();
+}
+
+rf_status rf_attn_fwd_rowwise(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Hkv, int Sq, int Sk, int d, float scale,
+                              int causal, const rf_blockmask* bm, rf_dtype dt, rf_stream stream) {
+  if (d != 64 && d != 128)
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd_rowwise: d must be 64 or 128, got %d", d);
+  rf::AttnArgs a{};
+  bool empty = false;
+  const rf_status pst = attn_prepare("rf_attn_fwd_rowwise", q, k, v, o, lse, B, H, Hkv, Sq, Sk,
+                                     d, scale, causal, bm, dt, a, &empty);
+  if (pst != RF_OK || empty) return pst;
+  cudaError_t e = rf::launch_attn_rowwise(a, dt, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_attn_fwd_rowwise: launch");
   return ok();
 }
 

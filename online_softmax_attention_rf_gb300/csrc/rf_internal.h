@@ -69,6 +69,7 @@ cudaError_t launch_softmax_rows(const void* x, void* y, int64_t rows, int64_t co
                                 bool skip_first_copy = false);
 cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attn_tc_bf16(const AttnArgs& a, cudaStream_t s, const char** why);
+cudaError_t launch_attn_rowwise(const AttnArgs& a, rf_dtype dt, cudaStream_t s);
 cudaError_t launch_decode_partials(const void* q, const void* k, const void* v, float* o_part,
                                    float* lse_part, int B, int H, int Hkv, int Sk, int d,
                                    float scale, int nsplit, cudaStream_t s, int* status);

@@ -39,6 +39,11 @@ WORKLOADS = {
     # first rows, which see every key)
     "two_level": dict(B=2, H=16, Hkv=16, Sq=16384, Sk=16384, d=64, causal=False,
                       dtype="bf16", seed=8, amp=1.0, band=256, n_global=64),
+    # short sequences under a scattered (Bigbird-like) element mask: window
+    # 16, 8 global tokens, 1 % random keys -- the row-wise kernel's regime
+    "scattered_short": dict(B=16, H=16, Hkv=16, Sq=1024, Sk=1024, d=64, causal=False,
+                            dtype="bf16", seed=11, amp=1.0, window=16, n_global=8,
+                            density=0.01),
 }
 
 #: Row-softmax shapes (rows, cols): one row fits a CTA; one row spans a cluster.
@@ -132,6 +137,16 @@ def band_global_mask(S, band, n_global, rows=None):
     return out
 
 
+def scattered_mask(S, window, n_global, density, seed):
+    """bool [S, S] element mask, Bigbird-like: keys within `window` of the
+    query row, `n_global` global tokens (first keys and first rows), and
+    random keys drawn independently with probability `density`."""
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    m = (np.abs(i - j) <= window) | (j < n_global) | (i < n_global)
+    return m | (np.random.default_rng(seed).random((S, S)) < density)
+
+
 def random_tile_mask(nqt, nkt, density, seed, nheads=None):
     """bool [nqt, nkt] (or [nheads, nqt, nkt]) with each tile present w.p. density."""
     rng = np.random.default_rng(seed)
@@ -150,4 +165,7 @@ def workload_inputs(name):
         extras["tile_mask"] = window_random_tile_mask(nqt, w["window"], w["frac"], w["seed"])
     if name == "two_level":
         extras["elem_mask"] = band_global_mask(w["Sq"], w["band"], w["n_global"])
+    if name == "scattered_short":
+        extras["elem_mask"] = scattered_mask(w["Sq"], w["window"], w["n_global"], w["density"],
+                                             w["seed"])
     return q, k, v, default_scale(w["d"]), extras
