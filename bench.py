@@ -50,6 +50,9 @@ TRAFFIC = {
     # attn_tc_kernel<64, 1> on two_level: dram__bytes.sum.per_second x duration
     "attn_tc_two_level": {"digest": "8dc32d453b50a32d", "bytes": 350505000,
                           "sources": ("attn_tc.cu", "rf_device.cuh")},
+    # attn_tc_kernel<64, 0> on block_sparse: dram read 201.5 MB + write 50.1 MB
+    "attn_tc_block_sparse": {"digest": "8dc32d453b50a32d", "bytes": 251527680,
+                             "sources": ("attn_tc.cu", "rf_device.cuh")},
     # softmax_rows kernels: dram__bytes_read.sum + dram__bytes_write.sum
     "softmax_rows_64k": {"digest": "78500a3290548dca", "bytes": 2087176704,
                          "sources": ("softmax_rows.cu", "rf_device.cuh")},
