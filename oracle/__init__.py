@@ -23,8 +23,9 @@ Modules
                  reaches the three-pass result; the same for the pairwise
                  merge of (count, mean, M2) moment states.
 ``cascades``     other cascaded reductions the pages name: top-k softmax
-                 routing of Mixture-of-Experts tokens, and per-row mean and
-                 variance (normalisation statistics).
+                 routing of Mixture-of-Experts tokens, per-row mean and
+                 variance (normalisation statistics), and the moment of
+                 inertia of point sets about their centre of mass.
 
 Every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` against brute force, closed forms, invariants
@@ -44,5 +45,11 @@ from .three_pass import (  # noqa: F401
     visible_mask,
     visited_tiles,
 )
-from .incremental import incremental_attention, moments_merge, moments_state  # noqa: F401
-from .cascades import moe_route, row_moments  # noqa: F401
+from .incremental import (  # noqa: F401
+    incremental_attention,
+    moments_merge,
+    moments_state,
+    weighted_merge,
+    weighted_state,
+)
+from .cascades import moe_route, moment_of_inertia, row_moments  # noqa: F401

@@ -24,6 +24,12 @@ Readings where the pages are silent (each listed in the design notes):
 * Row moments: mean = sum(x) / n, then var = sum((x - mean)^2) / n (the
   population variance, the one normalisation layers use); the normalised row
   is (x - mean) / sqrt(var + eps).
+* Moment of inertia (the Korean page's non-ML workload): for a set of point
+  masses m_i at positions r_i, the total mass M = sum m_i and the centre of
+  mass c = sum m_i r_i / M (reduction 1), then the moment of inertia about
+  the centre of mass, I = sum m_i |r_i - c|^2 (reduction 2, which needs c):
+  the scalar (polar) moment, the trace-free reading being the plainest one
+  for a workload given only by name.
 """
 
 import numpy as np
@@ -67,3 +73,22 @@ def row_moments(x, eps=1e-5):
     var = (d * d).sum(axis=1) / n                      # reduction 2, needs reduction 1
     y = d / np.sqrt(var + eps)[:, None]
     return mean, var, y
+
+
+def moment_of_inertia(points, masses=None):
+    """Per point set: total mass, centre of mass, and the moment of inertia
+    about the centre of mass, by the two-pass definition in float64.
+
+    points [S, N, k] (any float dtype, cast exactly), masses [S, N] (None:
+    unit masses). Returns (M [S], c [S, k], I [S]); a set of total mass 0
+    gives c = 0 and I = 0.
+    """
+    r = np.asarray(points, dtype=np.float64)
+    S, N, k = r.shape
+    m = np.ones((S, N)) if masses is None else np.asarray(masses, dtype=np.float64)
+    M = m.sum(axis=1)                                             # reduction 1
+    safe = np.where(M != 0, M, 1.0)
+    c = np.where((M != 0)[:, None], (m[:, :, None] * r).sum(axis=1) / safe[:, None], 0.0)
+    d = r - c[:, None, :]
+    I = np.where(M != 0, (m * (d * d).sum(axis=2)).sum(axis=1), 0.0)   # reduction 2
+    return M, c, I

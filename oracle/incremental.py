@@ -121,3 +121,29 @@ def moments_merge(a, b):
         return (0, 0.0, 0.0)
     delta = mb - ma
     return (n, ma + delta * nb / n, qa + qb + delta * delta * na * nb / n)
+
+
+def weighted_state(points, masses):
+    """(W, c, M2) of one chunk of point masses: W = sum m, c the weighted
+    mean position, M2 = sum m |r - c|^2 (two passes over the chunk)."""
+    r = np.asarray(points, dtype=np.float64).reshape(-1, np.shape(points)[-1])
+    m = np.asarray(masses, dtype=np.float64).reshape(-1)
+    W = m.sum()
+    if W == 0:
+        return (0.0, np.zeros(r.shape[1]), 0.0)
+    c = (m[:, None] * r).sum(axis=0) / W
+    return (W, c, float((m * ((r - c) ** 2).sum(axis=1)).sum()))
+
+
+def weighted_merge(a, b):
+    """Pairwise merge of (W, c, M2) states: the mass-weighted form of the
+    count merge above (weights in place of counts)."""
+    wa, ca, qa = a
+    wb, cb, qb = b
+    W = wa + wb
+    if wb == 0:
+        return a
+    if wa == 0:
+        return b
+    delta = np.asarray(cb) - np.asarray(ca)
+    return (W, ca + delta * (wb / W), qa + qb + float(delta @ delta) * wa * wb / W)

@@ -119,10 +119,79 @@ def test_moment_states_merge_to_the_two_pass_result(chunk):
     assert abs(l[1] - r[1]) < 1e-12 and abs(l[2] - r[2]) < 1e-8
 
 
+def _brute_inertia(points, masses):
+    """Python-math loops: total mass, centre of mass, then sum m |r - c|^2."""
+    M = math.fsum(masses)
+    k = len(points[0])
+    c = [math.fsum(m * p[j] for p, m in zip(points, masses)) / M for j in range(k)]
+    I = math.fsum(m * math.fsum((p[j] - c[j]) ** 2 for j in range(k))
+                  for p, m in zip(points, masses))
+    return M, c, I
+
+
+def test_inertia_brute_force():
+    rng = np.random.default_rng(7)
+    r = rng.normal(size=(3, 9, 3)) * 2 + 5
+    m = rng.random((3, 9)) + 0.1
+    M, c, I = oracle.moment_of_inertia(r, m)
+    for s in range(3):
+        bM, bc, bI = _brute_inertia(r[s].tolist(), m[s].tolist())
+        assert abs(M[s] - bM) < 1e-12 and np.allclose(c[s], bc, rtol=1e-13)
+        assert abs(I[s] - bI) < 1e-11 * bI
+
+
+def test_inertia_closed_forms():
+    # two point masses: I = m1 m2 / (m1 + m2) d^2
+    M, c, I = oracle.moment_of_inertia([[[0.0, 0.0, 0.0], [0.0, 0.0, 2.0]]], [[1.0, 3.0]])
+    assert M[0] == 4.0 and np.allclose(c[0], [0, 0, 1.5]) and abs(I[0] - 3.0) < 1e-14
+    # N unit masses on a circle of radius R: centre 0, I = N R^2
+    t = np.arange(12) * (2 * np.pi / 12)
+    ring = np.stack([3.0 * np.cos(t), 3.0 * np.sin(t), np.zeros(12)], axis=1)[None]
+    M, c, I = oracle.moment_of_inertia(ring)
+    assert np.allclose(c[0], 0, atol=1e-14) and abs(I[0] - 12 * 9.0) < 1e-12
+    # zero total mass
+    M, c, I = oracle.moment_of_inertia(np.ones((1, 4, 3)), np.zeros((1, 4)))
+    assert M[0] == 0 and np.all(c[0] == 0) and I[0] == 0
+
+
+def test_inertia_parallel_axis_translation_and_variance():
+    rng = np.random.default_rng(8)
+    r = rng.normal(size=(4, 50, 3)) + np.array([10.0, -4.0, 2.0])
+    m = rng.random((4, 50))
+    M, c, I = oracle.moment_of_inertia(r, m)
+    about_origin = (m * (r * r).sum(axis=2)).sum(axis=1)          # parallel-axis theorem
+    np.testing.assert_allclose(about_origin, I + M * (c * c).sum(axis=1), rtol=1e-12)
+    M2, c2, I2 = oracle.moment_of_inertia(r + 7.5, m)               # translation
+    np.testing.assert_allclose(I2, I, rtol=1e-10)
+    np.testing.assert_allclose(c2, c + 7.5, rtol=1e-13)
+    Mu, cu, Iu = oracle.moment_of_inertia(r)                          # unit masses
+    np.testing.assert_allclose(Iu, 50 * np.var(r, axis=1).sum(axis=1), rtol=1e-12)
+
+
+@pytest.mark.parametrize("chunk", [1, 5, 64])
+def test_weighted_states_merge_to_the_two_pass_result(chunk):
+    rng = np.random.default_rng(9)
+    r = rng.normal(size=(301, 3)) * 3 + 20
+    m = rng.random(301) + 0.01
+    st = (0.0, np.zeros(3), 0.0)
+    for c0 in range(0, 301, chunk):
+        st = oracle.weighted_merge(st, oracle.weighted_state(r[c0:c0 + chunk], m[c0:c0 + chunk]))
+    M, c, I = oracle.moment_of_inertia(r[None], m[None])
+    assert abs(st[0] - M[0]) < 1e-10 and np.allclose(st[1], c[0], rtol=1e-12)
+    assert abs(st[2] - I[0]) < 1e-9 * I[0]
+    a, b, d = (oracle.weighted_state(r[i:i + 100], m[i:i + 100]) for i in (0, 100, 200))
+    left = oracle.weighted_merge(oracle.weighted_merge(a, b), d)
+    right = oracle.weighted_merge(a, oracle.weighted_merge(b, d))
+    assert abs(left[2] - right[2]) < 1e-9 * left[2]
+
+
 def _pins():
     yield lambda: test_moe_route_brute_force(True)
     yield test_moe_route_ties_and_special_cases
     yield test_row_moments_library_and_closed_forms
+    yield test_inertia_brute_force
+    yield test_inertia_closed_forms
+    yield test_inertia_parallel_axis_translation_and_variance
 
 
 def _mutant_route_ties_upward(logits, k, renorm=False):
@@ -145,12 +214,29 @@ def _mutant_sample_variance(x, eps=1e-5):
     return mean, var, d / np.sqrt(var + eps)[:, None]
 
 
+def _mutant_inertia_about_origin(points, masses=None):
+    M, c, I = _orig_inertia(points, masses)
+    r = np.asarray(points, dtype=np.float64)
+    m = np.ones(r.shape[:2]) if masses is None else np.asarray(masses, dtype=np.float64)
+    return M, c, (m * (r * r).sum(axis=2)).sum(axis=1)
+
+
+def _mutant_inertia_unweighted_centre(points, masses=None):
+    r = np.asarray(points, dtype=np.float64)
+    m = np.ones(r.shape[:2]) if masses is None else np.asarray(masses, dtype=np.float64)
+    c = r.mean(axis=1)
+    return m.sum(axis=1), c, (m * ((r - c[:, None]) ** 2).sum(axis=2)).sum(axis=1)
+
+
 _orig_route = oc.moe_route
+_orig_inertia = oc.moment_of_inertia
 
 
 @pytest.mark.parametrize("target,mutant", [
     ("moe_route", _mutant_route_ties_upward), ("moe_route", _mutant_route_no_renorm),
-    ("row_moments", _mutant_sample_variance)])
+    ("row_moments", _mutant_sample_variance),
+    ("moment_of_inertia", _mutant_inertia_about_origin),
+    ("moment_of_inertia", _mutant_inertia_unweighted_centre)])
 def test_pins_catch_planted_mistakes(monkeypatch, target, mutant):
     monkeypatch.setattr(oracle, target, mutant)
     failures = 0
