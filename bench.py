@@ -58,12 +58,16 @@ TRAFFIC = {
                          "sources": ("softmax_rows.cu", "rf_device.cuh")},
     "softmax_rows_1m": {"digest": "78500a3290548dca", "bytes": 2088350208,
                         "sources": ("softmax_rows.cu", "rf_device.cuh")},
-    # moe_route_sorted_kernel<float, 8> and row_moments_smem_kernel<float>:
-    # dram__bytes_read.sum + dram__bytes_write.sum
-    "moe_route": {"digest": "8df86f5d7d516d0f", "bytes": 140411392,
+    # moe_route_sorted_kernel<float, 8>, row_moments_smem_kernel<float> and
+    # inertia_kernel: dram__bytes_read.sum + dram__bytes_write.sum (the first
+    # two were captured on digest 8df86f5d7d516d0f; the file has since only
+    # gained the inertia kernel, theirs is unchanged)
+    "moe_route": {"digest": "632f30d120f849b6", "bytes": 140411392,
                   "sources": ("cascades.cu", "rf_device.cuh")},
-    "row_moments": {"digest": "8df86f5d7d516d0f", "bytes": 1016724224,
+    "row_moments": {"digest": "632f30d120f849b6", "bytes": 1016724224,
                     "sources": ("cascades.cu", "rf_device.cuh")},
+    "inertia": {"digest": "632f30d120f849b6", "bytes": 1076813056,
+                "sources": ("cascades.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
     # (sources since then differ only by device helpers the kernel does not use)
     "decode_partials_decode_splitk": {"digest": "4c12c369bc05677a", "bytes": 4302000000,
@@ -393,6 +397,7 @@ def run_ours(args, dist, rank, world, local):
         "scattered_short": scattered,
         "moe_route": cascades["moe_route"],
         "row_moments": cascades["row_moments"],
+        "moment_of_inertia": cascades["moment_of_inertia"],
         "cpu_baseline": {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "%d whole heads of the workload (%.1f s, float64 three-pass "
                                    "NumPy oracle)" % (cpu_heads, cpu_dt)},
@@ -642,6 +647,32 @@ def bench_cascades(args, dev, stream, peaks, peak_src):
                      "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for("row_moments"),
                      "peak_source": "%s HBM copy" % peak_src}}
     del x, y, mean, var
+    c = inputs.CASCADE_WORKLOADS["inertia"]
+    pts, ms = inputs.make_point_sets(c["sets"], c["n"], c["seed"], c["amp"], c["offset"])
+    pts, ms = pts.to(dev), ms.to(dev)
+    total = torch.empty(c["sets"], dtype=torch.float32, device=dev)
+    centre = torch.empty(c["sets"], 3, dtype=torch.float32, device=dev)
+    inertia = torch.empty_like(total)
+    algo = pts.numel() * 4 + ms.numel() * 4 + c["sets"] * 5 * 4
+
+    def step_inertia():
+        api.lib().rf_moment_of_inertia(pts.data_ptr(), ms.data_ptr(), c["sets"], c["n"],
+                                       total.data_ptr(), centre.data_ptr(), inertia.data_ptr(),
+                                       api._stream())
+
+    # points and masses (1.07 GB) are far larger than L2: no flush needed
+    total_ms, per = time_steps(step_inertia, side_steps(args), args.warmup, stream, None)
+    ms_ = statistics.mean(per)
+    assert api.device_status() == 0
+    gbs = algo / (ms_ * 1e-3) / 1e9
+    out["moment_of_inertia"] = {
+        "workload": "moment_of_inertia [%d sets x %d points, 3-D, f32 masses]" % (c["sets"],
+                                                                               c["n"]),
+        "value": gbs, "unit": "GB/s", "ms_per_step": ms_, "algorithmic_bytes": algo,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for("inertia"),
+                     "peak_source": "%s HBM copy" % peak_src}}
+    del pts, ms, total, centre, inertia
     torch.cuda.empty_cache()
     return out
 

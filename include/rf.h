@@ -355,6 +355,26 @@ rf_status rf_row_moments(const void *x, int64_t rows, int64_t cols, float eps, f
                          float *var, void *y, rf_dtype dt, rf_stream stream);
 
 /*
+ * Moment of inertia of point sets (the Korean RedFuser page's results: a
+ * non-ML cascaded reduction): for each set of n point masses, the total mass
+ * M = sum m_i and the centre of mass c = sum m_i r_i / M (reduction 1), then
+ * the moment of inertia about the centre of mass I = sum m_i |r_i - c|^2
+ * (reduction 2, which needs c), in one read of the points: mass-weighted
+ * (W, c, M2) states merged pairwise (the weighted form of Chan, Golub and
+ * LeVeque's merge).
+ *  points : float [sets, n, 3] (x, y, z of each point), device.
+ *  masses : float [sets, n], device, or NULL for unit masses.
+ *  total_mass : float [sets]; center: float [sets, 3]; inertia: float [sets];
+ *               device, each may be NULL.
+ *  sets >= 0 (0: nothing launched), n >= 0; a set of total mass 0 (or
+ *  n = 0) gives M = 0, c = 0, I = 0. Errors: RF_ERR_INVALID for NULL points
+ *  with n > 0, negative sizes, or misaligned pointers.
+ */
+rf_status rf_moment_of_inertia(const float *points, const float *masses, int64_t sets, int64_t n,
+                               float *total_mass, float *center, float *inertia,
+                               rf_stream stream);
+
+/*
  * Test aid: when visited is non-NULL, every later rf_attn_fwd on this host
  * thread sets visited[((b*H + h) * nqt + qt) * nkt + kt] = 1 for each
  * 128 x 128 tile (qt, kt) whose scores it computes. The caller zeroes the

@@ -69,6 +69,7 @@ SIGNATURES = {
                                  ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "rf_moe_route": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _I, _P]),
     "rf_row_moments": (_I, [_P, _I64, _I64, _F, _P, _P, _P, _I, _P]),
+    "rf_moment_of_inertia": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
     "rf_debug_set_visited": (_I, [_P, _I64]),
     "rf_debug_inject_fault": (_I, [_I]),
     "rf_device_status": (_I, [_P, ctypes.POINTER(_I)]),
@@ -255,6 +256,23 @@ def row_moments(x, eps=1e-5, normalize=True, out=None):
     _check(lib().rf_row_moments(_ptr(x), rows, x.shape[1], float(eps), _ptr(mean), _ptr(var),
                                 _ptr(y), _dt(x), _stream()))
     return mean, var, y
+
+
+def moment_of_inertia(points, masses=None):
+    """rf_moment_of_inertia: points [sets, n, 3] float32 (+ masses [sets, n])
+    -> (total mass [sets], centre [sets, 3], inertia [sets])."""
+    _cuda(points, masses)
+    if points.dim() != 3 or points.shape[2] != 3 or points.dtype != torch.float32:
+        raise ValueError("points must be float32 [sets, n, 3]")
+    sets, n = points.shape[0], points.shape[1]
+    if masses is not None and (masses.shape != (sets, n) or masses.dtype != torch.float32):
+        raise ValueError("masses must be float32 [sets, n]")
+    total = torch.empty(sets, dtype=torch.float32, device=points.device)
+    centre = torch.empty(sets, 3, dtype=torch.float32, device=points.device)
+    inertia = torch.empty(sets, dtype=torch.float32, device=points.device)
+    _check(lib().rf_moment_of_inertia(_ptr(points), _ptr(masses), sets, n, _ptr(total),
+                                      _ptr(centre), _ptr(inertia), _stream()))
+    return total, centre, inertia
 
 
 def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,

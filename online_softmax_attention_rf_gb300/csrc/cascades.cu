@@ -29,6 +29,12 @@
 // shared memory, float rows of up to 32768 elements otherwise stay in
 // registers between the two (x is read once); longer rows are read a second
 // time, from L2, where the first pass left them with an evict-last policy.
+//
+// Moment of inertia (one CTA per point set; the Korean page's non-ML
+// workload): the total mass and centre of mass, then the sum of m |r - c|^2
+// about that centre, in one read of the points: mass-weighted (W, c, M2)
+// states of four points (two passes over registers), merged pairwise with
+// the masses as weights.
 #include "rf_device.cuh"
 
 namespace rf {
@@ -578,6 +584,119 @@ cudaError_t launch_moments_t(const T* x, int64_t rows, int64_t cols, float eps, 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ moment of inertia
+
+// (W, c, M2) of point masses: total mass, weighted mean position, and the
+// sum of m |r - c|^2.
+struct WMoments {
+  float w, cx, cy, cz, m2;
+};
+
+__device__ __forceinline__ WMoments wmerge(WMoments a, WMoments b) {
+  if (b.w == 0.f) return a;
+  if (a.w == 0.f) return b;
+  const float w = a.w + b.w, f = b.w / w;
+  const float dx = b.cx - a.cx, dy = b.cy - a.cy, dz = b.cz - a.cz;
+  return {w, a.cx + dx * f, a.cy + dy * f, a.cz + dz * f,
+          a.m2 + b.m2 + (dx * dx + dy * dy + dz * dz) * a.w * f};
+}
+
+__device__ __forceinline__ WMoments wshfl_merge(WMoments a, int o) {
+  WMoments b;
+  b.w = __shfl_xor_sync(0xffffffffu, a.w, o);
+  b.cx = __shfl_xor_sync(0xffffffffu, a.cx, o);
+  b.cy = __shfl_xor_sync(0xffffffffu, a.cy, o);
+  b.cz = __shfl_xor_sync(0xffffffffu, a.cz, o);
+  b.m2 = __shfl_xor_sync(0xffffffffu, a.m2, o);
+  return wmerge(a, b);
+}
+
+// Four point masses: two passes over registers (centre, then M2).
+__device__ __forceinline__ WMoments chunk4(const float (&x)[12], const float (&m)[4]) {
+  const float w = (m[0] + m[1]) + (m[2] + m[3]);
+  if (w == 0.f) return {0.f, 0.f, 0.f, 0.f, 0.f};
+  float sx = 0.f, sy = 0.f, sz = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    sx = fmaf(m[i], x[3 * i], sx);
+    sy = fmaf(m[i], x[3 * i + 1], sy);
+    sz = fmaf(m[i], x[3 * i + 2], sz);
+  }
+  const float inv = 1.f / w;
+  const float cx = sx * inv, cy = sy * inv, cz = sz * inv;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float dx = x[3 * i] - cx, dy = x[3 * i + 1] - cy, dz = x[3 * i + 2] - cz;
+    q = fmaf(m[i], dx * dx + dy * dy + dz * dz, q);
+  }
+  return {w, cx, cy, cz, q};
+}
+
+constexpr int kInertiaThreads = 256;
+
+// One CTA per point set. vec4: the set's points and masses start 16-byte
+// aligned and n % 4 == 0 (four points = three float4, four masses = one).
+__global__ void __launch_bounds__(kInertiaThreads) inertia_kernel(
+    const float* __restrict__ pts, const float* __restrict__ mass, int64_t n, int vec4,
+    float* __restrict__ total, float* __restrict__ centre, float* __restrict__ inertia) {
+  __shared__ WMoments part[kInertiaThreads / 32];
+  const int64_t set = blockIdx.x;
+  const float* ps = pts + set * n * 3;
+  const float* ms = mass != nullptr ? mass + set * n : nullptr;
+  const uint64_t drop = policy_evict_first();
+  WMoments st{0.f, 0.f, 0.f, 0.f, 0.f};
+  if (vec4) {
+#pragma unroll 2
+    for (int64_t c = threadIdx.x; c < n / 4; c += kInertiaThreads) {
+      float x[12], m[4];
+      const uint4* p4 = reinterpret_cast<const uint4*>(ps + c * 12);
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const uint4 u = ld_global_policy(p4 + j, drop);
+        x[4 * j] = __uint_as_float(u.x);
+        x[4 * j + 1] = __uint_as_float(u.y);
+        x[4 * j + 2] = __uint_as_float(u.z);
+        x[4 * j + 3] = __uint_as_float(u.w);
+      }
+      if (ms != nullptr) {
+        const uint4 u = ld_global_policy(reinterpret_cast<const uint4*>(ms + c * 4), drop);
+        m[0] = __uint_as_float(u.x);
+        m[1] = __uint_as_float(u.y);
+        m[2] = __uint_as_float(u.z);
+        m[3] = __uint_as_float(u.w);
+      } else {
+        m[0] = m[1] = m[2] = m[3] = 1.f;
+      }
+      st = wmerge(st, chunk4(x, m));
+    }
+  } else {
+    for (int64_t i = threadIdx.x; i < n; i += kInertiaThreads) {
+      const float mi = ms != nullptr ? ms[i] : 1.f;
+      st = wmerge(st, WMoments{mi, ps[3 * i], ps[3 * i + 1], ps[3 * i + 2], 0.f});
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) st = wshfl_merge(st, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = st;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    WMoments w = threadIdx.x < kInertiaThreads / 32 ? part[threadIdx.x]
+                                                     : WMoments{0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w = wshfl_merge(w, o);
+    if (threadIdx.x == 0) {
+      if (total != nullptr) total[set] = w.w;
+      if (centre != nullptr) {
+        centre[3 * set] = w.cx;
+        centre[3 * set + 1] = w.cy;
+        centre[3 * set + 2] = w.cz;
+      }
+      if (inertia != nullptr) inertia[set] = w.m2;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_moe_route(const void* logits, int64_t T_, int E, int k, int renorm,
@@ -599,6 +718,16 @@ cudaError_t launch_row_moments(const void* x, int64_t rows, int64_t cols, float 
                             static_cast<float*>(y), vec8, s);
   return launch_moments_t(static_cast<const __nv_bfloat16*>(x), rows, cols, eps, mean, var,
                           static_cast<__nv_bfloat16*>(y), vec8, s);
+}
+
+cudaError_t launch_moment_of_inertia(const float* points, const float* masses, int64_t sets,
+                                     int64_t n, float* total, float* centre, float* inertia,
+                                     cudaStream_t s) {
+  const bool vec4 = n % 4 == 0 && reinterpret_cast<uintptr_t>(points) % 16 == 0 &&
+                    (masses == nullptr || reinterpret_cast<uintptr_t>(masses) % 16 == 0);
+  inertia_kernel<<<static_cast<unsigned>(sets), kInertiaThreads, 0, s>>>(
+      points, masses, n, vec4 ? 1 : 0, total, centre, inertia);
+  return cudaGetLastError();
 }
 
 }  // namespace rf

@@ -380,4 +380,21 @@ rf_status rf_row_moments(const void* x, int64_t rows, int64_t cols, float eps, f
   return ok();
 }
 
+rf_status rf_moment_of_inertia(const float* points, const float* masses, int64_t sets,
+                               int64_t n, float* total_mass, float* center, float* inertia,
+                               rf_stream stream) {
+  if (sets < 0 || n < 0) return fail(RF_ERR_INVALID, "rf_moment_of_inertia: negative size");
+  if (sets > INT32_MAX) return fail(RF_ERR_INVALID, "rf_moment_of_inertia: sets > 2^31-1");
+  if (n > (int64_t(1) << 40)) return fail(RF_ERR_INVALID, "rf_moment_of_inertia: n too large");
+  if (sets == 0) return ok();
+  if (n > 0 && points == nullptr)
+    return fail(RF_ERR_INVALID, "rf_moment_of_inertia: points is NULL");
+  if (!aligned(points, 4) || !aligned(masses, 4))
+    return fail(RF_ERR_INVALID, "rf_moment_of_inertia: points and masses must be 4-byte aligned");
+  cudaError_t e = rf::launch_moment_of_inertia(points, masses, sets, n, total_mass, center,
+                                               inertia, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_moment_of_inertia: launch");
+  return ok();
+}
+
 }  // extern "C"

@@ -81,6 +81,9 @@ cudaError_t launch_blockmask_build(const uint8_t* dense, int nheads, int nqt, in
                                    cudaStream_t s, int* status);
 cudaError_t launch_moe_route(const void* logits, int64_t T, int E, int k, int renorm,
                              int32_t* idx, float* w, float* lse, rf_dtype dt, cudaStream_t s);
+cudaError_t launch_moment_of_inertia(const float* points, const float* masses, int64_t sets,
+                                     int64_t n, float* total, float* centre, float* inertia,
+                                     cudaStream_t s);
 cudaError_t launch_row_moments(const void* x, int64_t rows, int64_t cols, float eps, float* mean,
                                float* var, void* y, rf_dtype dt, cudaStream_t s);
 cudaError_t launch_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, int Sk,

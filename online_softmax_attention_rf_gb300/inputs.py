@@ -56,10 +56,13 @@ SOFTMAX_WORKLOADS = {
 #: for a 256-expert, top-8 model (float32 logits, N(0, amp^2)). Row moments:
 #: normalisation-layer rows (float32, N(offset, amp^2): a mean far from zero
 #: relative to the spread is the case a one-pass sum of squares gets wrong).
+#: Inertia: sets of point masses in 3-D.
 CASCADE_WORKLOADS = {
     "moe_route": dict(T=131072, E=256, k=8, renorm=True, dtype="f32", seed=9, amp=2.0),
     "row_moments": dict(rows=16384, cols=8192, dtype="f32", seed=10, amp=1.0, offset=8.0,
                         eps=1e-5),
+    # point sets: positions N(offset, amp^2) per coordinate, masses U(0.5, 1.5)
+    "inertia": dict(sets=2048, n=32768, seed=12, amp=2.0, offset=5.0),
 }
 
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -99,6 +102,14 @@ def make_logits(T, E, seed, dtype="f32", amp=1.0, ties=False):
 def make_moment_rows(rows, cols, seed, dtype="f32", amp=1.0, offset=0.0):
     g = torch.Generator().manual_seed(seed)
     return (torch.randn(rows, cols, generator=g) * amp + offset).to(TORCH_DTYPES[dtype])
+
+
+def make_point_sets(sets, n, seed, amp=1.0, offset=0.0):
+    """(points float32 [sets, n, 3], masses float32 [sets, n])."""
+    g = torch.Generator().manual_seed(seed)
+    points = torch.randn(sets, n, 3, generator=g) * amp + offset
+    masses = torch.rand(sets, n, generator=g) + 0.5
+    return points, masses
 
 
 def n_tiles(S, tile=128):

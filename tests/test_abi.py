@@ -217,3 +217,13 @@ def test_moe_route_and_moments_empty_are_no_ops(L):
     (4, 4, 1e-5, None, api.RF_F32), (4, 4, 1e-5, A, 9), (2 ** 31, 4, 1e-5, A, api.RF_F32)])
 def test_row_moments_rejects(L, rows, cols, eps, x, dt):
     assert L.rf_row_moments(x, rows, cols, eps, A, A, None, dt, None) == api.RF_ERR_INVALID
+
+
+def test_moment_of_inertia_validation(L):
+    f = L.rf_moment_of_inertia
+    assert f(A, A, -1, 4, A, A, A, None) == api.RF_ERR_INVALID
+    assert f(A, A, 4, -1, A, A, A, None) == api.RF_ERR_INVALID
+    assert f(None, A, 4, 4, A, A, A, None) == api.RF_ERR_INVALID
+    assert f(A + 2, A, 4, 4, A, A, A, None) == api.RF_ERR_INVALID
+    assert f(A, None, 2 ** 31, 4, A, A, A, None) == api.RF_ERR_INVALID
+    assert f(None, None, 0, 4, None, None, None, None) == api.RF_OK

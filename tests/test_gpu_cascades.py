@@ -178,3 +178,54 @@ def test_row_moments_full_size_sampled(cuda_device):
     assert api.device_status() == 0
     rows = np.random.default_rng(1).choice(c["rows"], 64, replace=False)
     _check_moments(x[rows], mean.cpu()[rows], var.cpu()[rows], y.cpu()[rows], c["eps"])
+
+
+def _check_inertia(points, masses, M, c, I):
+    """Bounds from float32 rounding: K u times the magnitudes involved
+    (u = 2^-24, K = 256 as above); sigma = sqrt(I / M) is the spread."""
+    rM, rc, rI = oracle.moment_of_inertia(f64(points), None if masses is None else f64(masses))
+    sig = np.sqrt(np.where(rM > 0, rI / np.where(rM > 0, rM, 1), 0))
+    cn = np.abs(rc).max(axis=1)
+    assert (np.abs(f64(M) - rM) <= K_GROWTH * U32 * rM + 1e-30).all()
+    tol_c = K_GROWTH * U32 * (cn + sig) + 1e-30
+    assert (np.abs(f64(c) - rc).max(axis=1) <= tol_c).all(), "centre"
+    tol_i = K_GROWTH * U32 * rI * (1 + cn / np.maximum(sig, 1e-30)) + 1e-30
+    err = np.abs(f64(I) - rI)
+    assert (err <= tol_i).all(), "inertia: worst err/tol %.3g" % (err / tol_i).max()
+
+
+@pytest.mark.parametrize("sets,n", [(5, 1), (7, 3), (3, 4), (4, 1000), (2, 4096), (3, 4097),
+                                    (8, 100000)])
+@pytest.mark.parametrize("unit", [False, True])
+def test_moment_of_inertia_matches_oracle(cuda_device, sets, n, unit):
+    points, masses = inputs.make_point_sets(sets, n, sets * 31 + n, amp=2.0, offset=5.0)
+    if unit:
+        masses = None
+    M, c, I = api.moment_of_inertia(points.cuda(), None if unit else masses.cuda())
+    assert api.device_status() == 0
+    _check_inertia(points, masses, M, c, I)
+
+
+def test_moment_of_inertia_zero_mass_and_unaligned(cuda_device):
+    points, masses = inputs.make_point_sets(3, 2049, 4, amp=1.0, offset=-3.0)
+    masses[1] = 0.0                                   # a set without mass
+    pd, md = points.cuda(), masses.cuda()
+    M, c, I = api.moment_of_inertia(pd, md)
+    assert api.device_status() == 0
+    assert M[1].item() == 0 and torch.all(c[1] == 0) and I[1].item() == 0
+    _check_inertia(points, masses, M, c, I)
+    # a view one point in (12-byte offset): the element-wise path
+    flat = pd.reshape(-1)[3:3 + 3 * 2048 * 3].view(3, 2048, 3)
+    mflat = md.reshape(-1)[1:1 + 3 * 2048].view(3, 2048)
+    M3, c3, I3 = api.moment_of_inertia(flat, mflat)
+    assert api.device_status() == 0
+    _check_inertia(flat.cpu(), mflat.cpu(), M3, c3, I3)
+
+
+def test_moment_of_inertia_full_size_sampled(cuda_device):
+    w = inputs.CASCADE_WORKLOADS["inertia"]
+    points, masses = inputs.make_point_sets(w["sets"], w["n"], w["seed"], w["amp"], w["offset"])
+    M, c, I = api.moment_of_inertia(points.cuda(), masses.cuda())
+    assert api.device_status() == 0
+    sets = np.random.default_rng(2).choice(w["sets"], 64, replace=False)
+    _check_inertia(points[sets], masses[sets], M.cpu()[sets], c.cpu()[sets], I.cpu()[sets])
