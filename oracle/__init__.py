@@ -24,8 +24,10 @@ Modules
                  merge of (count, mean, M2) moment states.
 ``cascades``     other cascaded reductions the pages name: top-k softmax
                  routing of Mixture-of-Experts tokens, per-row mean and
-                 variance (normalisation statistics), and the moment of
-                 inertia of point sets about their centre of mass.
+                 variance (normalisation statistics), the moment of
+                 inertia of point sets about their centre of mass, and
+                 per-row FP8 (E4M3) absmax quantisation with the GEMM over
+                 the quantised values.
 
 Every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` against brute force, closed forms, invariants
@@ -52,4 +54,13 @@ from .incremental import (  # noqa: F401
     weighted_merge,
     weighted_state,
 )
-from .cascades import moe_route, moment_of_inertia, row_moments  # noqa: F401
+from .cascades import (  # noqa: F401
+    E4M3_MAX,
+    e4m3_code,
+    e4m3_round,
+    fp8_gemm,
+    moe_route,
+    moment_of_inertia,
+    row_moments,
+    rowquant_e4m3,
+)

@@ -30,6 +30,16 @@ Readings where the pages are silent (each listed in the design notes):
   the centre of mass, I = sum m_i |r_i - c|^2 (reduction 2, which needs c):
   the scalar (polar) moment, the trace-free reading being the plainest one
   for a workload given only by name.
+* FP8 quantisation + GEMM (named only): per-row absmax quantisation to FP8
+  E4M3 (the format with 4 exponent bits, bias 7, 3 mantissa bits, largest
+  finite value 448, subnormals down to 2^-9): amax = max |x| over the row
+  (reduction 1); the row is scaled by 448 / amax and rounded to the nearest
+  E4M3 value, ties to even, magnitudes past 448 saturating to 448; the row's
+  dequantisation scale is amax / 448 (an all-zero row: codes 0, scale 1).
+  Because the rounding decides an integer code, it is taken in float32, as
+  the kernel computes it: inv = float32(448) / float32(amax), then
+  float32(x) * inv. The GEMM (reduction 2, over the quantised values) is
+  C[m, n] = sa[m] * sw[n] * sum_k qa[m, k] qw[n, k], in float64 here.
 """
 
 import numpy as np
@@ -92,3 +102,56 @@ def moment_of_inertia(points, masses=None):
     d = r - c[:, None, :]
     I = np.where(M != 0, (m * (d * d).sum(axis=2)).sum(axis=1), 0.0)   # reduction 2
     return M, c, I
+
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v):
+    """Nearest E4M3 value of float64 v (ties to even), saturating at 448,
+    from the format's definition: normal numbers 2^e (1 + m/8), e in
+    [-6, 8], subnormals m * 2^-9."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)                       # below 2^-6: the subnormal spacing 2^-9
+    quantum = np.exp2(e - 3)
+    q = np.round(a / quantum) * quantum         # numpy rounds halves to even
+    q = np.minimum(q, E4M3_MAX)
+    return np.sign(v) * q
+
+
+def e4m3_code(v):
+    """The 8-bit code (sign, exponent, mantissa) of E4M3 values."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    sign = (np.signbit(v) & (a > 0)).astype(np.uint8) << 7
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    normal = a >= 2.0 ** -6
+    exp_field = np.where(normal, e + 7, 0).astype(np.int64)
+    mant = np.where(normal, a / np.exp2(e) - 1.0, a / 2.0 ** -9) * np.where(normal, 8, 1)
+    return (sign | (exp_field << 3).astype(np.uint8) | np.rint(mant).astype(np.uint8)).astype(
+        np.uint8)
+
+
+def rowquant_e4m3(x):
+    """Per-row absmax quantisation of x [R, K] (any float dtype) to E4M3.
+    Returns (q float64 [R, K] of E4M3 values, scale float32 [R])."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x32).max(axis=1)                                    # reduction 1
+    safe = np.where(amax > 0, amax, np.float32(1.0)).astype(np.float32)
+    inv = (np.float32(E4M3_MAX) / safe).astype(np.float32)
+    prod = (x32 * inv[:, None]).astype(np.float32)                    # float32, as the kernel
+    q = e4m3_round(prod.astype(np.float64))
+    q = np.where((amax > 0)[:, None], q, 0.0)
+    scale = np.where(amax > 0, safe / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    return q, scale
+
+
+def fp8_gemm(qa, sa, qw, sw):
+    """C = diag(sa) (qa qw^T) diag(sw) in float64 (reduction 2 over k)."""
+    qa = np.asarray(qa, dtype=np.float64)
+    qw = np.asarray(qw, dtype=np.float64)
+    return (np.asarray(sa, np.float64)[:, None] * (qa @ qw.T)) * np.asarray(sw, np.float64)[None]

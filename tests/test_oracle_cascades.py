@@ -185,6 +185,68 @@ def test_weighted_states_merge_to_the_two_pass_result(chunk):
     assert abs(left[2] - right[2]) < 1e-9 * left[2]
 
 
+def _all_finite_e4m3():
+    """Every finite E4M3 value, decoded by torch's float8_e4m3fn (codes 0x7f
+    and 0xff are NaN)."""
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return codes, vals
+
+
+def test_e4m3_against_torch():
+    codes, vals = _all_finite_e4m3()
+    assert np.array_equal(oracle.e4m3_round(vals), vals)          # representable values stay
+    pos = vals >= 0
+    assert np.array_equal(oracle.e4m3_code(vals[pos & (vals > 0)]), codes[pos & (vals > 0)])
+    # midpoints between neighbours (ties to even) and random values in range
+    u = np.unique(np.abs(vals))
+    mids = (u[1:] + u[:-1]) / 2
+    rng = np.random.default_rng(10)
+    probe = np.concatenate([mids, -mids, rng.uniform(-448, 448, 2000),
+                            rng.uniform(-1, 1, 2000) * 2.0 ** -5])
+    want = torch.from_numpy(probe).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.e4m3_round(probe), want)
+
+
+def test_e4m3_saturates():
+    v = np.array([448.0, 449.0, 464.0, 480.0, 1e6, -1e30])
+    assert np.array_equal(oracle.e4m3_round(v), [448, 448, 448, 448, 448, -448])
+
+
+def test_rowquant_properties():
+    rng = np.random.default_rng(11)
+    x = (rng.normal(size=(6, 300)) * np.array([1e-3, 1, 7, 100, 3e4, 1])[:, None]).astype(np.float32)
+    x[5] = 0.0
+    q, sc = oracle.rowquant_e4m3(x)
+    assert np.all(np.abs(q[:5]).max(axis=1) == 448.0)              # the absmax element maps to 448
+    assert np.all(q[5] == 0) and sc[5] == 1.0
+    amax = np.abs(x[:5]).max(axis=1)
+    np.testing.assert_allclose(sc[:5], amax / 448.0, rtol=1e-7)
+    # dequantised error: half a unit in the last of 3 mantissa bits, or half
+    # the subnormal spacing, in units of the scale
+    err = np.abs(q[:5] * sc[:5, None] - x[:5])
+    bound = 2.0 ** -4 * np.abs(x[:5]) + 2.0 ** -10 * sc[:5, None] * 1.0001
+    assert np.all(err <= bound)
+    # exact scaling by a power of two leaves the codes unchanged
+    q2, sc2 = oracle.rowquant_e4m3(x * np.float32(8.0))
+    assert np.array_equal(q2, q) and np.allclose(sc2[:5], sc[:5] * 8, rtol=0)
+
+
+def test_fp8_gemm_definition():
+    rng = np.random.default_rng(12)
+    a = rng.normal(size=(5, 64)).astype(np.float32)
+    w = rng.normal(size=(3, 64)).astype(np.float32)
+    qa, sa = oracle.rowquant_e4m3(a)
+    qw, sw = oracle.rowquant_e4m3(w)
+    c = oracle.fp8_gemm(qa, sa, qw, sw)
+    for i in range(5):
+        for j in range(3):
+            ref = math.fsum(float(qa[i, k]) * float(qw[j, k]) for k in range(64))
+            assert abs(c[i, j] - float(sa[i]) * float(sw[j]) * ref) < 1e-9 * (1 + abs(c[i, j]))
+    np.testing.assert_allclose(c, (qa * sa[:, None]) @ (qw * sw[:, None]).T, rtol=1e-12)
+    np.testing.assert_allclose(c, a @ w.T, rtol=0.2, atol=2.0)   # close to the unquantised product
+
+
 def _pins():
     yield lambda: test_moe_route_brute_force(True)
     yield test_moe_route_ties_and_special_cases
@@ -192,6 +254,9 @@ def _pins():
     yield test_inertia_brute_force
     yield test_inertia_closed_forms
     yield test_inertia_parallel_axis_translation_and_variance
+    yield test_e4m3_against_torch
+    yield test_e4m3_saturates
+    yield test_rowquant_properties
 
 
 def _mutant_route_ties_upward(logits, k, renorm=False):
@@ -228,17 +293,39 @@ def _mutant_inertia_unweighted_centre(points, masses=None):
     return m.sum(axis=1), c, (m * ((r - c[:, None]) ** 2).sum(axis=2)).sum(axis=1)
 
 
+def _mutant_e4m3_half_away(v):
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.clip(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6, 8)
+    qn = np.exp2(e - 3)
+    return np.sign(v) * np.minimum(np.floor(a / qn + 0.5) * qn, 448.0)
+
+
+def _mutant_e4m3_no_saturation(v):
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.clip(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6, None)
+    qn = np.exp2(e - 3)
+    return np.sign(v) * np.round(a / qn) * qn
+
+
 _orig_route = oc.moe_route
 _orig_inertia = oc.moment_of_inertia
+_orig_e4m3 = oc.e4m3_round
 
 
 @pytest.mark.parametrize("target,mutant", [
     ("moe_route", _mutant_route_ties_upward), ("moe_route", _mutant_route_no_renorm),
     ("row_moments", _mutant_sample_variance),
     ("moment_of_inertia", _mutant_inertia_about_origin),
-    ("moment_of_inertia", _mutant_inertia_unweighted_centre)])
+    ("moment_of_inertia", _mutant_inertia_unweighted_centre),
+    ("e4m3_round", _mutant_e4m3_half_away), ("e4m3_round", _mutant_e4m3_no_saturation)])
 def test_pins_catch_planted_mistakes(monkeypatch, target, mutant):
     monkeypatch.setattr(oracle, target, mutant)
+    if target == "e4m3_round":      # rowquant_e4m3 calls it through its own module
+        monkeypatch.setattr(oc, target, mutant)
     failures = 0
     for pin in _pins():
         try:
