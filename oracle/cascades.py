@@ -119,14 +119,15 @@ def e4m3_round(v):
     quantum = np.exp2(e - 3)
     q = np.round(a / quantum) * quantum         # numpy rounds halves to even
     q = np.minimum(q, E4M3_MAX)
-    return np.sign(v) * q
+    return np.copysign(q, v)                    # zeros keep their sign
 
 
 def e4m3_code(v):
-    """The 8-bit code (sign, exponent, mantissa) of E4M3 values."""
+    """The 8-bit code (sign, exponent, mantissa) of E4M3 values; the sign bit
+    is kept for zero (a negative value that rounds to zero is -0, 0x80)."""
     v = np.asarray(v, dtype=np.float64)
     a = np.abs(v)
-    sign = (np.signbit(v) & (a > 0)).astype(np.uint8) << 7
+    sign = np.signbit(v).astype(np.uint8) << 7
     with np.errstate(divide="ignore"):
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     normal = a >= 2.0 ** -6

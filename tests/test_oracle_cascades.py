@@ -206,6 +206,10 @@ def test_e4m3_against_torch():
                             rng.uniform(-1, 1, 2000) * 2.0 ** -5])
     want = torch.from_numpy(probe).to(torch.float8_e4m3fn).to(torch.float64).numpy()
     assert np.array_equal(oracle.e4m3_round(probe), want)
+    # codes of everything, signs and signed zeros included (tiny values round to +-0)
+    probe = np.concatenate([probe, [-1e-5, 1e-5, -0.0, 0.0], -vals[vals > 0]])
+    codes_t = torch.from_numpy(probe).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_code(oracle.e4m3_round(probe)), codes_t)
 
 
 def test_e4m3_saturates():
