@@ -398,6 +398,8 @@ def run_ours(args, dist, rank, world, local):
         "moe_route": cascades["moe_route"],
         "row_moments": cascades["row_moments"],
         "moment_of_inertia": cascades["moment_of_inertia"],
+        "fp8_quant": cascades["fp8_quant"],
+        "fp8_gemm": cascades["fp8_gemm"],
         "cpu_baseline": {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "%d whole heads of the workload (%.1f s, float64 three-pass "
                                    "NumPy oracle)" % (cpu_heads, cpu_dt)},
@@ -673,6 +675,50 @@ def bench_cascades(args, dev, stream, peaks, peak_src):
                      "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for("inertia"),
                      "peak_source": "%s HBM copy" % peak_src}}
     del pts, ms, total, centre, inertia
+    # FP8: per-row quantisation of the activations, then the GEMM over codes
+    c = inputs.CASCADE_WORKLOADS["fp8_gemm"]
+    a_h, w_h = inputs.make_gemm_operands(c["M"], c["N"], c["K"], c["seed"])
+    a, wt = a_h.to(dev), w_h.to(dev)
+    qa = torch.empty(c["M"], c["K"], dtype=torch.uint8, device=dev)
+    sa = torch.empty(c["M"], dtype=torch.float32, device=dev)
+    qw, sw = api.rowquant_e4m3(wt)            # weights: quantised once
+    cm = torch.empty(c["M"], c["N"], dtype=torch.bfloat16, device=dev)
+
+    def step_quant():
+        api.lib().rf_rowquant_e4m3(a.data_ptr(), c["M"], c["K"], qa.data_ptr(), sa.data_ptr(),
+                                   api.RF_BF16, api._stream())
+
+    def step_gemm():
+        api.lib().rf_fp8_gemm(qa.data_ptr(), sa.data_ptr(), qw.data_ptr(), sw.data_ptr(),
+                              cm.data_ptr(), c["M"], c["N"], c["K"], api._stream())
+
+    # A (128 MiB bf16) + codes (64 MiB) exceed L2 for the quantiser; the GEMM
+    # reads 128 MiB of codes and writes 128 MiB of C per launch
+    _, per_q = time_steps(step_quant, side_steps(args), args.warmup, stream, None)
+    _, per_g = time_steps(step_gemm, side_steps(args), args.warmup, stream, None)
+    assert api.device_status() == 0
+    ms_q, ms_g = statistics.mean(per_q), statistics.mean(per_g)
+    qbytes = a.numel() * 2 + qa.numel() + sa.numel() * 4
+    flops = 2.0 * c["M"] * c["N"] * c["K"]
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    tf = flops / (ms_g * 1e-3) / 1e12
+    out["fp8_quant"] = {
+        "workload": "rowquant_e4m3 [%d x %d] bf16 -> E4M3 codes + row scales" % (c["M"], c["K"]),
+        "value": qbytes / (ms_q * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_q,
+        "algorithmic_bytes": qbytes,
+        "roofline": {"bound": "hbm", "achieved": qbytes / (ms_q * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": qbytes / (ms_q * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": traffic_for("rowquant"), "peak_source": "%s HBM copy" % peak_src}}
+    out["fp8_gemm"] = {
+        "workload": "fp8_gemm E4M3 [M=%d, N=%d, K=%d] -> bf16, row and column scales" % (
+            c["M"], c["N"], c["K"]),
+        "value": tf, "unit": "TFLOP/s", "ms_per_step": ms_g, "ms_with_quant": ms_g + ms_q,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": tf / fp8_peak, "traffic": traffic_for("fp8_gemm"),
+                     "peak_source": "%s dense bf16 (burst) x 2, the nominal fp8/bf16 ratio"
+                                    % peak_src}}
+    del a, wt, qa, sa, qw, sw, cm
     torch.cuda.empty_cache()
     return out
 

@@ -375,6 +375,38 @@ rf_status rf_moment_of_inertia(const float *points, const float *masses, int64_t
                                rf_stream stream);
 
 /*
+ * Per-row FP8 quantisation (RedFuser page, sections 1 and 4: FP8 quantisation
+ * followed by GEMM is a cascade of reductions). For each row of x:
+ * amax = max |x| (reduction 1); codes = E4M3(float32(x) * (448 / amax)),
+ * rounded to nearest even and saturated at 448 (4 exponent bits, bias 7,
+ * 3 mantissa bits); scale = amax / 448. An all-zero row gives codes 0 and
+ * scale 1. The row is read once (staged in shared memory).
+ *  x     : [rows, K] row-major, RF_F32 or RF_BF16, device, 16-byte aligned.
+ *  q     : uint8 [rows, K] E4M3 codes, device, 16-byte aligned.
+ *  scale : float [rows], device.
+ *  rows >= 0 (0: nothing launched); K a positive multiple of 16 with
+ *  K * element size <= 64 KB (RF_ERR_UNSUPPORTED otherwise).
+ */
+rf_status rf_rowquant_e4m3(const void *x, int64_t rows, int64_t K, uint8_t *q, float *scale,
+                           rf_dtype dt, rf_stream stream);
+
+/*
+ * GEMM over E4M3 codes with per-row and per-column scales (reduction 2 of the
+ * cascade above): C[m, n] = sa[m] * sw[n] * sum_k A[m, k] W[n, k], products
+ * accumulated in float32 by tcgen05.mma kind::f8f6f4 tiles of 128 x 256, C
+ * rounded to bf16.
+ *  a  : uint8 [M, K] codes (K-major), w: uint8 [N, K] codes (K-major),
+ *       c: bf16 [M, N]; device, 16-byte aligned.
+ *  sa : float [M], sw: float [N]; device.
+ *  M a multiple of 128, N of 256, K a positive multiple of 128
+ *  (RF_ERR_UNSUPPORTED otherwise); M or N = 0: nothing launched.
+ * Errors: RF_ERR_INVALID for NULL or misaligned pointers; a device wait that
+ * gives up records RF_ERR_TIMEOUT in the device status word.
+ */
+rf_status rf_fp8_gemm(const uint8_t *a, const float *sa, const uint8_t *w, const float *sw,
+                      void *c, int M, int N, int K, rf_stream stream);
+
+/*
  * Test aid: when visited is non-NULL, every later rf_attn_fwd on this host
  * thread sets visited[((b*H + h) * nqt + qt) * nkt + kt] = 1 for each
  * 128 x 128 tile (qt, kt) whose scores it computes. The caller zeroes the

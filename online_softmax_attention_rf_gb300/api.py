@@ -70,6 +70,8 @@ SIGNATURES = {
     "rf_moe_route": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _I, _P]),
     "rf_row_moments": (_I, [_P, _I64, _I64, _F, _P, _P, _P, _I, _P]),
     "rf_moment_of_inertia": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
+    "rf_rowquant_e4m3": (_I, [_P, _I64, _I64, _P, _P, _I, _P]),
+    "rf_fp8_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "rf_debug_set_visited": (_I, [_P, _I64]),
     "rf_debug_inject_fault": (_I, [_I]),
     "rf_device_status": (_I, [_P, ctypes.POINTER(_I)]),
@@ -273,6 +275,33 @@ def moment_of_inertia(points, masses=None):
     _check(lib().rf_moment_of_inertia(_ptr(points), _ptr(masses), sets, n, _ptr(total),
                                       _ptr(centre), _ptr(inertia), _stream()))
     return total, centre, inertia
+
+
+def rowquant_e4m3(x):
+    """rf_rowquant_e4m3: x [rows, K] float32/bf16 -> (codes uint8 [rows, K],
+    scale float32 [rows])."""
+    _cuda(x)
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, K]")
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(x.shape[0], dtype=torch.float32, device=x.device)
+    _check(lib().rf_rowquant_e4m3(_ptr(x), x.shape[0], x.shape[1], _ptr(q), _ptr(sc), _dt(x),
+                                  _stream()))
+    return q, sc
+
+
+def fp8_gemm(a, sa, w, sw, out=None):
+    """rf_fp8_gemm: codes a [M, K], w [N, K] (uint8), scales sa [M], sw [N]
+    -> C bf16 [M, N]."""
+    _cuda(a, sa, w, sw)
+    M, K = a.shape
+    N = w.shape[0]
+    if w.shape[1] != K or a.dtype != torch.uint8 or w.dtype != torch.uint8:
+        raise ValueError("a [M, K] and w [N, K] must be uint8 codes")
+    c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device) if out is None else out
+    _cuda(c)
+    _check(lib().rf_fp8_gemm(_ptr(a), _ptr(sa), _ptr(w), _ptr(sw), _ptr(c), M, N, K, _stream()))
+    return c
 
 
 def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,

@@ -397,4 +397,47 @@ rf_status rf_moment_of_inertia(const float* points, const float* masses, int64_t
   return ok();
 }
 
+rf_status rf_rowquant_e4m3(const void* x, int64_t rows, int64_t K, uint8_t* q, float* scale,
+                           rf_dtype dt, rf_stream stream) {
+  if (rows < 0 || K < 0) return fail(RF_ERR_INVALID, "rf_rowquant_e4m3: negative size");
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_rowquant_e4m3: bad dtype");
+  if (rows == 0) return ok();
+  if (K == 0 || K % 16 != 0) return fail(RF_ERR_UNSUPPORTED, "rf_rowquant_e4m3: K must be a positive multiple of 16");
+  if (K * (dt == RF_F32 ? 4 : 2) > 64 * 1024)
+    return fail(RF_ERR_UNSUPPORTED, "rf_rowquant_e4m3: rows longer than 64 KB");
+  if (rows > INT32_MAX) return fail(RF_ERR_INVALID, "rf_rowquant_e4m3: rows > 2^31-1");
+  if (x == nullptr || q == nullptr || scale == nullptr)
+    return fail(RF_ERR_INVALID, "rf_rowquant_e4m3: NULL pointer");
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4))
+    return fail(RF_ERR_INVALID, "rf_rowquant_e4m3: x and q must be 16-byte aligned");
+  cudaError_t e = rf::launch_rowquant_e4m3(x, rows, K, q, scale, dt,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_rowquant_e4m3: launch");
+  return ok();
+}
+
+rf_status rf_fp8_gemm(const uint8_t* a, const float* sa, const uint8_t* w, const float* sw, void* c,
+                      int M, int N, int K, rf_stream stream) {
+  if (M < 0 || N < 0 || K < 0) return fail(RF_ERR_INVALID, "rf_fp8_gemm: negative size");
+  if (M == 0 || N == 0) return ok();
+  if (M % 128 != 0 || N % 256 != 0 || K % 128 != 0 || K == 0)
+    return fail(RF_ERR_UNSUPPORTED,
+                "rf_fp8_gemm: M must be a multiple of 128, N of 256, K a positive multiple of 128");
+  if (a == nullptr || sa == nullptr || w == nullptr || sw == nullptr || c == nullptr)
+    return fail(RF_ERR_INVALID, "rf_fp8_gemm: NULL pointer");
+  if (!aligned(a, 16) || !aligned(w, 16) || !aligned(c, 16) || !aligned(sa, 4) || !aligned(sw, 4))
+    return fail(RF_ERR_INVALID, "rf_fp8_gemm: a, w, c must be 16-byte aligned");
+  if (int64_t(M / 128) * (N / 256) > INT32_MAX)
+    return fail(RF_ERR_INVALID, "rf_fp8_gemm: too many tiles");
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_fp8_gemm: no CUDA device");
+  const char* why = nullptr;
+  cudaError_t e = rf::launch_fp8_gemm(a, sa, w, sw, c, M, N, K,
+                                      reinterpret_cast<cudaStream_t>(stream), st, &why);
+  if (e != cudaSuccess && why != nullptr)
+    return fail(RF_ERR_CUDA, "rf_fp8_gemm: %s: %s", why, cudaGetErrorString(e));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_fp8_gemm: launch");
+  return ok();
+}
+
 }  // extern "C"

@@ -23,7 +23,8 @@ enum DevKernel : int {
   kKerAttnTc = 3,
   kKerDecode = 4,
   kKerMerge = 5,
-  kKerBlockmask = 6
+  kKerBlockmask = 6,
+  kKerFp8 = 7
 };
 
 __host__ __device__ constexpr int dev_code(int kind, int kernel, int site) {
@@ -79,6 +80,11 @@ cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void
 cudaError_t launch_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
                                    int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
                                    cudaStream_t s, int* status);
+cudaError_t launch_rowquant_e4m3(const void* x, int64_t rows, int64_t K, uint8_t* q, float* scale,
+                                 rf_dtype dt, cudaStream_t s);
+cudaError_t launch_fp8_gemm(const uint8_t* a, const float* sa, const uint8_t* w, const float* sw,
+                            void* c, int M, int N, int K, cudaStream_t s, int* status,
+                            const char** why);
 cudaError_t launch_moe_route(const void* logits, int64_t T, int E, int k, int renorm,
                              int32_t* idx, float* w, float* lse, rf_dtype dt, cudaStream_t s);
 cudaError_t launch_moment_of_inertia(const float* points, const float* masses, int64_t sets,

@@ -63,6 +63,9 @@ CASCADE_WORKLOADS = {
                         eps=1e-5),
     # point sets: positions N(offset, amp^2) per coordinate, masses U(0.5, 1.5)
     "inertia": dict(sets=2048, n=32768, seed=12, amp=2.0, offset=5.0),
+    # a linear layer in FP8: activations A [M, K] and weights W [N, K], bf16
+    # N(0, 1) before per-row quantisation
+    "fp8_gemm": dict(M=8192, N=8192, K=8192, seed=13),
 }
 
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -102,6 +105,14 @@ def make_logits(T, E, seed, dtype="f32", amp=1.0, ties=False):
 def make_moment_rows(rows, cols, seed, dtype="f32", amp=1.0, offset=0.0):
     g = torch.Generator().manual_seed(seed)
     return (torch.randn(rows, cols, generator=g) * amp + offset).to(TORCH_DTYPES[dtype])
+
+
+def make_gemm_operands(M, N, K, seed, dtype="bf16"):
+    """(A [M, K], W [N, K]) drawn N(0, 1) on the CPU, in that order."""
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randn(M, K, generator=g).to(TORCH_DTYPES[dtype])
+    w = torch.randn(N, K, generator=g).to(TORCH_DTYPES[dtype])
+    return a, w
 
 
 def make_point_sets(sets, n, seed, amp=1.0, offset=0.0):

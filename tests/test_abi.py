@@ -227,3 +227,20 @@ def test_moment_of_inertia_validation(L):
     assert f(A + 2, A, 4, 4, A, A, A, None) == api.RF_ERR_INVALID
     assert f(A, None, 2 ** 31, 4, A, A, A, None) == api.RF_ERR_INVALID
     assert f(None, None, 0, 4, None, None, None, None) == api.RF_OK
+
+
+def test_fp8_validation(L):
+    q = L.rf_rowquant_e4m3
+    assert q(A, 4, 100, A, A, api.RF_BF16, None) == api.RF_ERR_UNSUPPORTED       # K % 16
+    assert q(A, 4, 65536, A, A, api.RF_BF16, None) == api.RF_ERR_UNSUPPORTED     # > 64 KB
+    assert q(A, 4, 64, A, A, 9, None) == api.RF_ERR_INVALID
+    assert q(None, 4, 64, A, A, api.RF_BF16, None) == api.RF_ERR_INVALID
+    assert q(MIS, 4, 64, A, A, api.RF_BF16, None) == api.RF_ERR_INVALID
+    assert q(None, 0, 64, None, None, api.RF_BF16, None) == api.RF_OK
+    g = L.rf_fp8_gemm
+    assert g(A, A, A, A, A, 100, 256, 128, None) == api.RF_ERR_UNSUPPORTED
+    assert g(A, A, A, A, A, 128, 128, 128, None) == api.RF_ERR_UNSUPPORTED
+    assert g(A, A, A, A, A, 128, 256, 100, None) == api.RF_ERR_UNSUPPORTED
+    assert g(None, A, A, A, A, 128, 256, 128, None) == api.RF_ERR_INVALID
+    assert g(MIS, A, A, A, A, 128, 256, 128, None) == api.RF_ERR_INVALID
+    assert g(None, None, None, None, None, 0, 256, 128, None) == api.RF_OK
