@@ -68,6 +68,12 @@ TRAFFIC = {
                     "sources": ("cascades.cu", "rf_device.cuh")},
     "inertia": {"digest": "632f30d120f849b6", "bytes": 1076813056,
                 "sources": ("cascades.cu", "rf_device.cuh")},
+    # fp8_gemm_kernel (persistent) and rowquant_kernel<bf16> on the 8192^3
+    # workload: dram__bytes_read.sum + dram__bytes_write.sum
+    "fp8_gemm": {"digest": "1bd446f9ea742eee", "bytes": 443226624,
+                 "sources": ("fp8_gemm.cu", "rf_device.cuh")},
+    "rowquant": {"digest": "1bd446f9ea742eee", "bytes": 167583744,
+                 "sources": ("fp8_gemm.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
     # (sources since then differ only by device helpers the kernel does not use)
     "decode_partials_decode_splitk": {"digest": "4c12c369bc05677a", "bytes": 4302000000,
