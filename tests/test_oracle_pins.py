@@ -287,6 +287,23 @@ def test_sdpa_top_left_causal_square():
     _close(o, ot.numpy())
 
 
+def test_sdpa_latent_kv_heads():
+    """Multi-head latent attention decode as the oracle computes it: many
+    query heads against one key head whose first dv columns are the values
+    (d_qk = latent + rope, d_v = latent), pinned by torch's SDPA with the
+    key head broadcast and v the key's leading columns."""
+    B, H, Sk, d, dv = 2, 8, 150, 24, 16
+    q = _rand((B, H, 1, d), 33)
+    kv = _rand((B, 1, Sk, d), 34)
+    o, lse = oracle.attention(q, kv, kv[..., :dv], 0.2)
+    tq = torch.from_numpy(q)
+    tk = torch.from_numpy(kv).expand(B, H, Sk, d)
+    ot = torch.nn.functional.scaled_dot_product_attention(tq, tk, tk[..., :dv], scale=0.2)
+    _close(o, ot.numpy())
+    s = 0.2 * (tq @ tk.transpose(-1, -2))
+    _close(lse, torch.logsumexp(s, dim=-1).numpy())
+
+
 def test_sdpa_lower_right_causal():
     # bottom-right alignment for Sq != Sk, pinned by torch's causal_lower_right
     from torch.nn.attention.bias import causal_lower_right
