@@ -304,12 +304,13 @@ def run_ours(args, dist, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
     if args.only in ("decode", "softmax", "softmax_long", "block_sparse", "two_level",
-                     "scattered", "cascades"):
+                     "scattered", "mla", "cascades"):
         # one workload alone (used for profiling captures)
         fn = {"decode": bench_decode, "softmax": bench_softmax,
               "softmax_long": lambda *a: bench_softmax(*a, name="rows_1m"),
               "block_sparse": bench_block_sparse, "two_level": bench_two_level,
-              "scattered": bench_scattered, "cascades": bench_cascades}[args.only]
+              "scattered": bench_scattered, "mla": bench_mla,
+              "cascades": bench_cascades}[args.only]
         out = fn(args, dev, stream, peaks, peak_src)
         if rank == 0:
             print(json.dumps(out), flush=True)
@@ -375,6 +376,7 @@ def run_ours(args, dist, rank, world, local):
     block_sparse = bench_block_sparse(args, dev, stream, peaks, peak_src)
     two_level = bench_two_level(args, dev, stream, peaks, peak_src)
     scattered = bench_scattered(args, dev, stream, peaks, peak_src)
+    mla = bench_mla(args, dev, stream, peaks, peak_src)
     cascades = bench_cascades(args, dev, stream, peaks, peak_src)
     launches = args.steps
 
@@ -401,6 +403,7 @@ def run_ours(args, dist, rank, world, local):
         "block_sparse": block_sparse,
         "two_level": two_level,
         "scattered_short": scattered,
+        "mla_decode": mla,
         "moe_route": cascades["moe_route"],
         "row_moments": cascades["row_moments"],
         "moment_of_inertia": cascades["moment_of_inertia"],
@@ -522,6 +525,43 @@ def bench_scattered(args, dev, stream, peaks, peak_src):
                         "traffic": None, "peak_source": "%s dense bf16 (burst)" % peak_src,
                         "note": "flops over visible pairs only"}}
     del q, k, v, o, lse, bm
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_mla(args, dev, stream, peaks, peak_src):
+    """MLA decode (absorbed form, B = 32, Sk = 8192, 128 heads, 576 / 512
+    columns): partials on the tensor cores + the log-sum-exp merge."""
+    from online_softmax_attention_rf_gb300 import api
+    w = inputs.MLA_WORKLOADS["mla_decode"]
+    q_h, kv_h = inputs.make_mla(w["B"], w["Sk"], w["seed"], w["amp"])
+    q, kv = q_h.to(dev), kv_h.to(dev)
+    o = torch.empty(w["B"], 128, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w["B"], 128, dtype=torch.float32, device=dev)
+    nb = api.lib().rf_mla_decode_workspace_bytes(w["B"], w["nsplit"])
+    ws = torch.empty(nb // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        api.mla_decode(q, kv, w["nsplit"], w["scale"], ws, o, lse)
+
+    # the latent cache (302 MB) is larger than L2: no flush needed
+    _, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    ms = statistics.mean(per)
+    assert api.device_status() == 0
+    flops = 2.0 * w["B"] * w["Sk"] * 128 * (576 + 512)
+    algo = kv.numel() * 2 + q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {"workload": "mla_decode [B=32, Sk=8192, 128 heads, d_qk 576, d_v 512, 16 splits]",
+           "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+           "gbs": algo / (ms * 1e-3) / 1e9, "algorithmic_bytes": algo,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                        "hbm_frac": algo / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "traffic": traffic_for("mla_decode"),
+                        "peak_source": "%s dense bf16 (burst)" % peak_src,
+                        "note": "flops count Q K^T over 576 columns and P V over 512 once; "
+                                "the two value halves recompute the scores (1.53x the MMAs)"}}
+    del q, kv, o, lse, ws
     torch.cuda.empty_cache()
     return out
 
@@ -736,7 +776,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax", "softmax_long",
-                                       "block_sparse", "two_level", "scattered", "cascades"],
+                                       "block_sparse", "two_level", "scattered", "mla",
+                                       "cascades"],
                     default="all",
                     help="time one workload alone (for profiling); the default runs all")
     args = ap.parse_args()

@@ -317,6 +317,30 @@ int rf_attn_estimate_us(int B, int H, int Sq, int Sk, int d, int64_t listed_tile
                         double *block_us, double *row_us);
 
 /*
+ * Multi-head latent attention (MLA) decode, absorbed form (RedFuser page,
+ * section 4: MLA is one of the evaluated workloads, compared with FlashMLA;
+ * section 3: multi-segment strategy). Each batch element has one query
+ * token of 128 heads and one latent key-value head:
+ *  q   : bf16 [B, 128, 576] (512 latent + 64 rotary columns per head);
+ *  kv  : bf16 [B, Sk, 576], shared by the 128 heads; the values are its
+ *        first 512 columns;
+ *  o   : bf16 [B, 128, 512]; lse: float [B, 128] (natural log) or NULL;
+ *  s = scale * q . kv over all 576 columns; o = softmax(s) v.
+ * The keys are cut into nsplit contiguous segments (floor(Sk/nsplit) keys,
+ * the last one takes the remainder; 1 <= nsplit <= Sk); per segment and per
+ * half of the value columns one CTA computes the partial (O, LSE) on the
+ * tensor cores, and the partials are merged by log-sum-exp (rf_splitk_merge)
+ * in the caller's workspace (float, >= rf_mla_decode_workspace_bytes bytes:
+ * o_part [B*128, nsplit, 512] then lse_part [B*128, nsplit]). All pointers
+ * device, 16-byte aligned (lse 4). Errors: RF_ERR_INVALID for bad sizes,
+ * NULL or misaligned pointers, a short workspace; a device wait that gives
+ * up records RF_ERR_TIMEOUT in the device status word.
+ */
+size_t rf_mla_decode_workspace_bytes(int B, int nsplit);
+rf_status rf_mla_decode(const void *q, const void *kv, void *o, float *lse, int B, int Sk,
+                        float scale, int nsplit, float *ws, size_t ws_bytes, rf_stream stream);
+
+/*
  * Mixture-of-Experts top-k softmax routing (RedFuser page, section 1: MoE
  * routing is a cascade of reductions; section 4: one of its workloads).
  * For each token t: p = softmax(logits[t, :]) over the E experts (maximum,

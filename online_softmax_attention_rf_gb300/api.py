@@ -71,6 +71,8 @@ SIGNATURES = {
     "rf_row_moments": (_I, [_P, _I64, _I64, _F, _P, _P, _P, _I, _P]),
     "rf_moment_of_inertia": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
     "rf_rowquant_e4m3": (_I, [_P, _I64, _I64, _P, _P, _I, _P]),
+    "rf_mla_decode_workspace_bytes": (_SZ, [_I, _I]),
+    "rf_mla_decode": (_I, [_P, _P, _P, _P, _I, _I, _F, _I, _P, _SZ, _P]),
     "rf_fp8_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "rf_debug_set_visited": (_I, [_P, _I64]),
     "rf_debug_inject_fault": (_I, [_I]),
@@ -302,6 +304,25 @@ def fp8_gemm(a, sa, w, sw, out=None):
     _cuda(c)
     _check(lib().rf_fp8_gemm(_ptr(a), _ptr(sa), _ptr(w), _ptr(sw), _ptr(c), M, N, K, _stream()))
     return c
+
+
+def mla_decode(q, kv, nsplit, scale, workspace=None, out=None, lse=None):
+    """rf_mla_decode: q [B, 128, 576], kv [B, Sk, 576] bf16 -> (o [B, 128, 512]
+    bf16, lse [B, 128] float32)."""
+    _cuda(q, kv)
+    B, Sk = kv.shape[0], kv.shape[1]
+    if q.shape != (B, 128, 576) or kv.shape[2] != 576:
+        raise ValueError("q must be [B, 128, 576] and kv [B, Sk, 576]")
+    o = torch.empty(B, 128, 512, dtype=torch.bfloat16, device=q.device) if out is None else out
+    if lse is None:
+        lse = torch.empty(B, 128, dtype=torch.float32, device=q.device)
+    nbytes = int(lib().rf_mla_decode_workspace_bytes(B, nsplit))
+    ws = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device=q.device) \
+        if workspace is None else workspace
+    _cuda(o, lse, ws)
+    _check(lib().rf_mla_decode(_ptr(q), _ptr(kv), _ptr(o), _ptr(lse), B, Sk, float(scale),
+                               int(nsplit), _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+    return o, lse
 
 
 def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=None,

@@ -440,4 +440,42 @@ rf_status rf_fp8_gemm(const uint8_t* a, const float* sa, const uint8_t* w, const
   return ok();
 }
 
+size_t rf_mla_decode_workspace_bytes(int B, int nsplit) {
+  return rf_decode_workspace_bytes(B, 128, nsplit, 512);
+}
+
+rf_status rf_mla_decode(const void* q, const void* kv, void* o, float* lse, int B, int Sk,
+                        float scale, int nsplit, float* ws, size_t ws_bytes, rf_stream stream) {
+  if (B < 1 || Sk < 1) return fail(RF_ERR_INVALID, "rf_mla_decode: bad sizes");
+  if (nsplit < 1 || nsplit > Sk) return fail(RF_ERR_INVALID, "rf_mla_decode: need 1 <= nsplit <= Sk");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(RF_ERR_INVALID, "rf_mla_decode: scale must be finite and > 0");
+  if (int64_t(B) * nsplit * 2 > INT32_MAX) return fail(RF_ERR_INVALID, "rf_mla_decode: too many splits");
+  if (int64_t(B) * Sk * 576 * 2 > (int64_t(1) << 46))
+    return fail(RF_ERR_INVALID, "rf_mla_decode: tensors too large");
+  if (q == nullptr || kv == nullptr || o == nullptr || ws == nullptr)
+    return fail(RF_ERR_INVALID, "rf_mla_decode: NULL pointer");
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(o, 16) || !aligned(ws, 16))
+    return fail(RF_ERR_INVALID, "rf_mla_decode: pointers must be 16-byte aligned");
+  if (lse != nullptr && !aligned(lse, 4))
+    return fail(RF_ERR_INVALID, "rf_mla_decode: lse must be 4-byte aligned");
+  if (ws_bytes < rf_mla_decode_workspace_bytes(B, nsplit))
+    return fail(RF_ERR_INVALID, "rf_mla_decode: workspace too small (%zu < %zu)", ws_bytes,
+                rf_mla_decode_workspace_bytes(B, nsplit));
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "rf_mla_decode: no CUDA device");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* o_part = ws;
+  float* lse_part = ws + size_t(B) * 128 * nsplit * 512;
+  const char* why = nullptr;
+  cudaError_t e = rf::launch_mla_decode_partials(q, kv, o_part, lse_part, B, Sk, nsplit, scale, s,
+                                                 st, &why);
+  if (e != cudaSuccess && why != nullptr)
+    return fail(RF_ERR_CUDA, "rf_mla_decode: %s: %s", why, cudaGetErrorString(e));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_mla_decode: partials launch");
+  e = rf::launch_splitk_merge(o_part, lse_part, o, lse, int64_t(B) * 128, nsplit, 512, RF_BF16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_mla_decode: merge launch");
+  return ok();
+}
+
 }  // extern "C"

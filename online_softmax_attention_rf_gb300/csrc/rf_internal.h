@@ -24,7 +24,8 @@ enum DevKernel : int {
   kKerDecode = 4,
   kKerMerge = 5,
   kKerBlockmask = 6,
-  kKerFp8 = 7
+  kKerFp8 = 7,
+  kKerMla = 8
 };
 
 __host__ __device__ constexpr int dev_code(int kind, int kernel, int site) {
@@ -85,6 +86,9 @@ cudaError_t launch_rowquant_e4m3(const void* x, int64_t rows, int64_t K, uint8_t
 cudaError_t launch_fp8_gemm(const uint8_t* a, const float* sa, const uint8_t* w, const float* sw,
                             void* c, int M, int N, int K, cudaStream_t s, int* status,
                             const char** why);
+cudaError_t launch_mla_decode_partials(const void* q, const void* kv, float* o_part,
+                                       float* lse_part, int B, int Sk, int nsplit, float scale,
+                                       cudaStream_t s, int* status, const char** why);
 cudaError_t launch_moe_route(const void* logits, int64_t T, int E, int k, int renorm,
                              int32_t* idx, float* w, float* lse, rf_dtype dt, cudaStream_t s);
 cudaError_t launch_moment_of_inertia(const float* points, const float* masses, int64_t sets,

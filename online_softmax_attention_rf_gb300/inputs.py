@@ -68,6 +68,14 @@ CASCADE_WORKLOADS = {
     "fp8_gemm": dict(M=8192, N=8192, K=8192, seed=13),
 }
 
+#: MLA decode, absorbed form: 128 query heads of one token against one latent
+#: head (512 latent + 64 rotary columns), values = the latent columns; scale
+#: 1 / sqrt(128 + 64) (the unabsorbed query-key dimension).
+MLA_WORKLOADS = {
+    "mla_decode": dict(B=32, Sk=8192, nsplit=16, seed=14, amp=1.0,
+                       scale=1.0 / math.sqrt(192.0)),
+}
+
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -113,6 +121,14 @@ def make_gemm_operands(M, N, K, seed, dtype="bf16"):
     a = torch.randn(M, K, generator=g).to(TORCH_DTYPES[dtype])
     w = torch.randn(N, K, generator=g).to(TORCH_DTYPES[dtype])
     return a, w
+
+
+def make_mla(B, Sk, seed, amp=1.0):
+    """(q bf16 [B, 128, 576], kv bf16 [B, Sk, 576]) drawn N(0, amp^2), q first."""
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, 128, 576, generator=g) * amp).to(torch.bfloat16)
+    kv = (torch.randn(B, Sk, 576, generator=g) * amp).to(torch.bfloat16)
+    return q, kv
 
 
 def make_point_sets(sets, n, seed, amp=1.0, offset=0.0):

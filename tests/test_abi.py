@@ -244,3 +244,15 @@ def test_fp8_validation(L):
     assert g(None, A, A, A, A, 128, 256, 128, None) == api.RF_ERR_INVALID
     assert g(MIS, A, A, A, A, 128, 256, 128, None) == api.RF_ERR_INVALID
     assert g(None, None, None, None, None, 0, 256, 128, None) == api.RF_OK
+
+
+def test_mla_decode_validation(L):
+    ws = L.rf_mla_decode_workspace_bytes(2, 4)
+    assert ws == (2 * 128 * 4 * 513 * 4 + 255) // 256 * 256
+    f = L.rf_mla_decode
+    assert f(A, A, A, A, 0, 64, 0.1, 1, A, ws, None) == api.RF_ERR_INVALID       # B
+    assert f(A, A, A, A, 2, 64, 0.1, 65, A, ws, None) == api.RF_ERR_INVALID      # nsplit > Sk
+    assert f(A, A, A, A, 2, 64, -1.0, 4, A, ws, None) == api.RF_ERR_INVALID      # scale
+    assert f(None, A, A, A, 2, 64, 0.1, 4, A, ws, None) == api.RF_ERR_INVALID
+    assert f(MIS, A, A, A, 2, 64, 0.1, 4, A, ws, None) == api.RF_ERR_INVALID
+    assert f(A, A, A, A, 2, 64, 0.1, 4, A, ws - 256, None) == api.RF_ERR_INVALID  # workspace
