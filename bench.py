@@ -74,6 +74,9 @@ TRAFFIC = {
                  "sources": ("fp8_gemm.cu", "rf_device.cuh")},
     "rowquant": {"digest": "1bd446f9ea742eee", "bytes": 167583744,
                  "sources": ("fp8_gemm.cu", "rf_device.cuh")},
+    # mla_decode_kernel on the MLA workload: dram read 306.9 MB + write 102.8 MB
+    "mla_decode": {"digest": "68dfa35ccfdc00b3", "bytes": 409670912,
+                   "sources": ("mla_decode.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
     # (sources since then differ only by device helpers the kernel does not use)
     "decode_partials_decode_splitk": {"digest": "4c12c369bc05677a", "bytes": 4302000000,
