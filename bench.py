@@ -53,6 +53,10 @@ TRAFFIC = {
     # attn_tc_kernel<64, 0> on block_sparse: dram read 201.5 MB + write 50.1 MB
     "attn_tc_block_sparse": {"digest": "8dc32d453b50a32d", "bytes": 251527680,
                              "sources": ("attn_tc.cu", "rf_device.cuh")},
+    # attn_tc_kernel<64, 1> (the selected block-wise kernel) on scattered_short:
+    # dram read 100.9 MB + write 11.8 MB
+    "attn_tc_scattered_short": {"digest": "8dc32d453b50a32d", "bytes": 112646656,
+                                "sources": ("attn_tc.cu", "rf_device.cuh")},
     # softmax_rows kernels: dram__bytes_read.sum + dram__bytes_write.sum
     "softmax_rows_64k": {"digest": "78500a3290548dca", "bytes": 2087176704,
                          "sources": ("softmax_rows.cu", "rf_device.cuh")},
@@ -525,7 +529,9 @@ def bench_scattered(args, dev, stream, peaks, peak_src):
            "listed_tiles": counts[0], "partial_tiles": counts[1], "visible_pairs": counts[2],
            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
-                        "traffic": None, "peak_source": "%s dense bf16 (burst)" % peak_src,
+                        "traffic": traffic_for("attn_tc_scattered_short") if chosen == "block"
+                        else None,
+                        "peak_source": "%s dense bf16 (burst)" % peak_src,
                         "note": "flops over visible pairs only"}}
     del q, k, v, o, lse, bm
     torch.cuda.empty_cache()
