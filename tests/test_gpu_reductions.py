@@ -112,12 +112,14 @@ def test_softmax_rows_edge_values(cuda_device):
     assert_close(xc, y_ref, TOL_F32, "y in place")
 
 
-@pytest.mark.parametrize("cols", [262144, 600000])
+@pytest.mark.parametrize("cols", [40000, 262144, 600000])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_softmax_rows_long_rows_masked_in_place(cuda_device, cols, dtype):
-    """Long rows take the cluster paths (on chip up to 16 slices, streaming
-    beyond): whole slices of -inf, a row with one visible entry and a row with
-    none must combine correctly, in place as well."""
+    """Rows longer than 64 KB take the cluster path (2 to 8 CTAs per row, each
+    streaming its slice twice; 40000 columns give clusters of 3 (f32) and 2
+    (bf16), the longer rows clusters of 8): whole slices of -inf, a row with
+    one visible entry and a row with none must combine correctly, in place as
+    well."""
     x = inputs.make_rows(3, cols, cols + 11, dtype, 3.0)
     x[0, cols // 3:] = -math.inf          # later CTAs see only -inf
     x[1, :] = -math.inf                   # nothing visible: zeros
