@@ -105,13 +105,13 @@ typedef struct {
 /*
  * Row softmax: y[r, :] = exp(x[r, :] - max) / sum(exp(x[r, :] - max)).
  * The pure two-reduction cascade of the RedFuser page's problem statement
- * (maximum, then sum of exponentials), one read and one write of x per
- * element in HBM: a row that fits one CTA (up to 64 KB: cols <= 16384 for
- * f32) is held in shared memory between the reductions and the write; a
- * longer row is split over a cluster of 2..16 CTAs (about 64 KB each) that
- * exchange (max, sum) pairs through distributed shared memory (multi-segment
- * strategy) and read their slice a second time from L2, where the first
- * read left it.
+ * (maximum, then sum of exponentials). A row that fits one CTA (up to
+ * 64 KB: cols <= 16384 for f32) is held in shared memory between the
+ * reductions and the write: one read and one write of x per element in HBM.
+ * A longer row is split over a cluster of 2..8 CTAs (64 KB or more each).
+ * They exchange (max, sum) pairs through distributed shared memory
+ * (multi-segment strategy), then read their slice a second time, mostly from
+ * L2 where the first read left it.
  *  x, y : [rows, cols] row-major, dtype dt (RF_F32 or RF_BF16); may alias.
  *  rows >= 0, cols >= 0 (either 0: nothing is launched, RF_OK).
  * A row whose entries are all -inf yields zeros. Errors: RF_ERR_INVALID for
