@@ -64,14 +64,12 @@ TRAFFIC = {
     "softmax_rows_1m": {"digest": "500902232009bba1", "bytes": 2417586176,
                         "sources": ("softmax_rows.cu", "rf_device.cuh")},
     # moe_route_sorted_kernel<float, 8>, row_moments_smem_kernel<float> and
-    # inertia_kernel: dram__bytes_read.sum + dram__bytes_write.sum (the first
-    # two were captured on digest 8df86f5d7d516d0f; the file has since only
-    # gained the inertia kernel, theirs is unchanged)
-    "moe_route": {"digest": "632f30d120f849b6", "bytes": 140411392,
+    # inertia_kernel: dram__bytes_read.sum + dram__bytes_write.sum
+    "moe_route": {"digest": "b54809b53ed0e0ac", "bytes": 139782656,
                   "sources": ("cascades.cu", "rf_device.cuh")},
-    "row_moments": {"digest": "632f30d120f849b6", "bytes": 1016724224,
+    "row_moments": {"digest": "b54809b53ed0e0ac", "bytes": 1016471552,
                     "sources": ("cascades.cu", "rf_device.cuh")},
-    "inertia": {"digest": "632f30d120f849b6", "bytes": 1076813056,
+    "inertia": {"digest": "b54809b53ed0e0ac", "bytes": 1076627200,
                 "sources": ("cascades.cu", "rf_device.cuh")},
     # fp8_gemm_kernel (persistent) and rowquant_kernel<bf16> on the 8192^3
     # workload: dram__bytes_read.sum + dram__bytes_write.sum

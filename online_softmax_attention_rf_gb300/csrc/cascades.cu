@@ -122,10 +122,12 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const T* __restrict__ lo
   // reduction 1: the maximum (the first round's winning key)
   uint32_t wk = __reduce_max_sync(0xffffffffu, k1);
   const float m = key_value(wk);
-  // reduction 2: sum of exp(x - m) (exp(-inf) = 0 for padding)
+  // reduction 2: sum of exp(x - m) (exp(-inf) = 0 for padding). x - m is
+  // rounded once before the scaling by log2 e, so the hardware exp2 keeps a
+  // relative error near 1e-6 even when the logits are far from zero.
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) s += expf(x[i] - m);
+  for (int i = 0; i < EPL; ++i) s += ex2_approx((x[i] - m) * kLog2e);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   // reduction 3, k rounds: the largest remaining key, then the lowest expert
@@ -216,10 +218,10 @@ __global__ void __launch_bounds__(256) moe_route_sorted_kernel(
   // reduction 1: the maximum (the first round's winning key)
   uint32_t wk = __reduce_max_sync(0xffffffffu, key[0]);
   const float m = key_value(wk);
-  // reduction 2: sum of exp(x - m)
+  // reduction 2: sum of exp(x - m), as in moe_route_kernel
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) s += expf(x[i] - m);
+  for (int i = 0; i < EPL; ++i) s += ex2_approx((x[i] - m) * kLog2e);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   // reduction 3, k rounds (every remaining key is >= 1, so an exhausted
