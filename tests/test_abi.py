@@ -256,3 +256,21 @@ def test_mla_decode_validation(L):
     assert f(None, A, A, A, 2, 64, 0.1, 4, A, ws, None) == api.RF_ERR_INVALID
     assert f(MIS, A, A, A, 2, 64, 0.1, 4, A, ws, None) == api.RF_ERR_INVALID
     assert f(A, A, A, A, 2, 64, 0.1, 4, A, ws - 256, None) == api.RF_ERR_INVALID  # workspace
+
+
+def test_no_cpu_fallback(L, monkeypatch):
+    """The binding computes nothing itself. Without the library every call
+    raises, and host tensors are refused rather than computed on the CPU."""
+    import torch
+    x = torch.randn(4, 8)
+    with pytest.raises(ValueError):
+        api.softmax_rows(x)
+    q = torch.randn(1, 1, 4, 64).to(torch.bfloat16)
+    with pytest.raises(ValueError):
+        api.attn_fwd(q, q, q)
+    monkeypatch.setattr(api, "_LIB", None)
+    monkeypatch.setattr(api, "library_path", lambda: os.path.join(ROOT, "no_such_dir", "librf.so"))
+    with pytest.raises(RuntimeError):
+        api.lib()
+    with pytest.raises(RuntimeError):
+        api.decode_workspace_bytes(1, 1, 1, 64)
