@@ -1,16 +1,16 @@
 """Benchmark of the fused online-softmax attention path on GB300.
 
-One step = one attention forward (rf_attn_fwd) over the causal multi-head
-prefill workload: B=4, H=32, Sq=Sk=4096, d=128, bf16 in / fp32 accumulate,
-inputs seeded-synthetic and resident in HBM. The JSON line reports
+One step = one attention forward (rf_attn_fwd) over the grouped-query,
+long-context causal prefill: B=1, Hq=64, Hkv=8, Sq=Sk=32768, d=128, bf16 in /
+fp32 accumulate, inputs seeded-synthetic and resident in HBM (the largest
+single-GPU configuration of the metric). The JSON line reports
   value      algorithmic TFLOP/s (4*d flops per visible query-key pair),
   e2e        the same metric through the public API with host buffers
              (pinned host -> device copies of Q, K, V and device -> host
              copies of O and LSE inside the timed region),
   roofline   the attention kernel against the measured dense bf16 peak,
-  decode     the split-K decode workload (B=16, Hq=32, Hkv=8, Sk=65536,
-             32 splits) in GB/s against the measured HBM copy bandwidth,
-  softmax    row softmax over a [16384 x 16384] fp32 matrix in GB/s,
+  mha_prefill, tiny_fp32, decode, softmax, ...   the other workloads, each
+             timed for at least MIN_SIDE_S seconds of launches,
   cpu_baseline  the float64 oracle on the host cores on a bounded sample.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -38,7 +38,12 @@ import torch  # noqa: E402
 
 from online_softmax_attention_rf_gb300 import inputs  # noqa: E402
 
-WORKLOAD = "mha_prefill"
+WORKLOAD = "gqa_long"
+# the metric as the workload statement names it; both arms print it verbatim
+METRIC = "attn fwd TFLOP/s & % BF16 tensor peak (prefill); decode GB/s & % HBM peak"
+# every secondary workload is timed for at least this long (clock sampling
+# and a stable mean), whatever --steps says
+MIN_SIDE_S = 0.5
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch from ncu captures (summarised under profiles/), valid only for the
@@ -149,7 +154,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -217,62 +222,82 @@ def barrier(dist):
 _INPUT_CACHE = {}
 
 
-def cpu_oracle_sample(name, budget_s=12.0):
-    """Time the float64 oracle on whole heads of the workload until the budget
-    is spent; returns (TFLOP/s, seconds, heads, cores)."""
+def cpu_oracle_sample(name, budget_s=12.0, start=0):
+    """Time the float64 oracle on query-row blocks of the workload until the
+    budget is spent; returns (TFLOP/s, seconds, blocks, cores).
+
+    A block is ROW_BLOCK consecutive query rows of one head. For causal
+    attention with Sq = Sk, rows [r0, r1) of a head see exactly keys [0, r1),
+    so the oracle runs on q[r0:r1] against k, v[:r1] (bottom-right alignment
+    makes that the same problem). Blocks are taken round-robin over heads and
+    spread over the rows, starting at block `start`; the flops counted are
+    the block's visible pairs, 4*d each."""
     import oracle
     w = inputs.WORKLOADS[name]
     if name not in _INPUT_CACHE:
         _INPUT_CACHE[name] = inputs.workload_inputs(name)
     q, k, v, scale, extras = _INPUT_CACHE[name]
-    tm = extras.get("tile_mask")
+    assert not extras and (not w["causal"] or w["Sq"] == w["Sk"])
     G = w["H"] // w["Hkv"]
-    pairs = visible_pairs(w, tm)
+    rb = oracle.three_pass.ROW_BLOCK
+    nrb = -(-w["Sq"] // rb)
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
     cores = len(os.sched_getaffinity(0))
-    t0 = time.perf_counter()
-    heads = 0
-    for b in range(w["B"]):
-        for h in range(w["H"]):
-            oracle.attention(q[b:b + 1, h:h + 1].double().numpy(),
-                             k[b:b + 1, h // G:h // G + 1].double().numpy(),
-                             v[b:b + 1, h // G:h // G + 1].double().numpy(), scale, w["causal"], tm)
-            heads += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    flops = 4.0 * w["d"] * pairs * heads
-    return flops / dt / 1e12, dt, heads, cores
+    spent, flops, blocks = 0.0, 0.0, 0
+    n = start
+    while spent < budget_s:
+        b, h = heads[n % len(heads)]
+        r0 = ((n // len(heads)) * 37 + n) % nrb * rb      # spread over the rows
+        r1 = min(w["Sq"], r0 + rb)
+        kend = r1 if w["causal"] else w["Sk"]
+        qb = q[b:b + 1, h:h + 1, r0:r1].double().numpy()
+        kb = k[b:b + 1, h // G:h // G + 1, :kend].double().numpy()
+        vb = v[b:b + 1, h // G:h // G + 1, :kend].double().numpy()
+        t0 = time.perf_counter()
+        oracle.attention(qb, kb, vb, scale, w["causal"])
+        spent += time.perf_counter() - t0
+        rows = np.arange(r0, r1, dtype=np.int64)
+        pairs = int((rows + 1).sum()) if w["causal"] else (r1 - r0) * w["Sk"]
+        flops += 4.0 * w["d"] * pairs
+        blocks += 1
+        n += 1
+    return flops / spent / 1e12, spent, blocks, cores
+
+
+def workload_config(name, world):
+    w = inputs.WORKLOADS[name]
+    return {"workload": name, "B": w["B"], "H": w["H"], "Hkv": w["Hkv"], "Sq": w["Sq"],
+            "Sk": w["Sk"], "d": w["d"], "causal": w["causal"],
+            "parallelism": "dp%d (independent replicas)" % world}
 
 
 def run_reference(args, dist, rank):
     """The oracle as the reference arm, on the host cores."""
     if rank != 0:
         return
-    w = inputs.WORKLOADS[WORKLOAD]
-    vals = []
     for _ in range(args.warmup):
-        cpu_oracle_sample(WORKLOAD, budget_s=2.0)
+        cpu_oracle_sample(WORKLOAD, budget_s=1.0)
     t0 = time.perf_counter()
-    samples = []
+    vals, samples = [], []
     per_step = min(8.0, 150.0 / args.steps)
-    for _ in range(args.steps):
-        v, dt, heads, cores = cpu_oracle_sample(WORKLOAD, budget_s=per_step)
+    cores = len(os.sched_getaffinity(0))
+    for s in range(args.steps):
+        v, dt, blocks, cores = cpu_oracle_sample(WORKLOAD, budget_s=per_step, start=1000 * s)
         vals.append(v)
-        samples.append(heads)
+        samples.append(blocks)
     elapsed = time.perf_counter() - t0
     value = statistics.median(vals)
     line = {
-        "impl": "reference", "metric": "attn fwd TFLOP/s (prefill)", "value": value,
+        "impl": "reference", "metric": METRIC, "value": value,
         "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * elapsed / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, **{kk: w[kk] for kk in ("B", "H", "Hkv", "Sq", "Sk", "d",
-                                                               "causal")}},
+        "config": workload_config(WORKLOAD, 1),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "whole heads of the workload per step (%s heads), float64 "
-                                   "three-pass NumPy oracle" % samples},
+                         "sample": "per step, %.1f s of 256-query-row blocks of the workload's "
+                                   "heads (blocks per step: %s), float64 three-pass NumPy "
+                                   "oracle; TFLOP/s over the blocks' visible pairs"
+                                   % (per_step, samples)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -302,27 +327,12 @@ def time_steps(fn, steps, warmup, stream, dist):
     return total_ms, per_launch
 
 
-def run_ours(args, dist, rank, world, local):
+def bench_prefill(name, args, dev, stream, peaks, peak_src, steps, warmup, dist=None, clk=None):
+    """Dense or causal prefill of a named workload: exactly `steps` timed
+    launches after `warmup`; returns (summary, inputs kept for e2e)."""
     from online_softmax_attention_rf_gb300 import api
-    api.lib()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream(dev)
-    peaks, peak_src = load_peaks()
-    if args.only in ("decode", "softmax", "softmax_long", "block_sparse", "two_level",
-                     "scattered", "mla", "cascades"):
-        # one workload alone (used for profiling captures)
-        fn = {"decode": bench_decode, "softmax": bench_softmax,
-              "softmax_long": lambda *a: bench_softmax(*a, name="rows_1m"),
-              "block_sparse": bench_block_sparse, "two_level": bench_two_level,
-              "scattered": bench_scattered, "mla": bench_mla,
-              "cascades": bench_cascades}[args.only]
-        out = fn(args, dev, stream, peaks, peak_src)
-        if rank == 0:
-            print(json.dumps(out), flush=True)
-        return
-    w = inputs.WORKLOADS[WORKLOAD]
-    q_h, k_h, v_h, scale, _ = inputs.workload_inputs(WORKLOAD)
+    w = inputs.WORKLOADS[name]
+    q_h, k_h, v_h, scale, _ = inputs.workload_inputs(name)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
@@ -331,27 +341,93 @@ def run_ours(args, dist, rank, world, local):
     def step():
         api.attn_fwd(q, k, v, scale, w["causal"], None, o, lse)
 
-    with ClockSampler(local) as clk:
-        total_ms, per_launch = time_steps(step, args.steps, args.warmup, stream, dist)
-    total_ms = max_over_ranks(dist, total_ms)
-    ms_step = total_ms / args.steps
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    if clk is not None:
+        with clk:
+            total_ms, per_launch = time_steps(step, steps, warmup, stream, dist)
+    else:
+        total_ms, per_launch = time_steps(step, steps, warmup, stream, dist)
     assert api.device_status() == 0
-
     att_ms = statistics.mean(per_launch)
     achieved = flops / (att_ms * 1e-3) / 1e12
-    traffic = traffic_for("attn_tc_mha_prefill")
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    out_bytes = o.numel() * o.element_size() + lse.numel() * 4
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": traffic_for("attn_tc_" + name),
+                "algorithmic_bytes": in_bytes + out_bytes,
                 "peak_source": "%s dense bf16 (burst)" % peak_src,
                 "frac_sustained": achieved / peaks.get("bf16_tflops_sustained",
                                                        peaks["bf16_tflops"])}
+    out = {"workload": name, "value": flops / (total_ms / steps * 1e-3) / 1e12,
+           "unit": "TFLOP/s", "ms_per_step": total_ms / steps, "total_ms": total_ms,
+           "flops_per_step": flops, "steps": steps, "roofline": roofline}
     del q, k, v, o, lse
     torch.cuda.empty_cache()
+    return out, (q_h, k_h, v_h, scale, w)
+
+
+def bench_tiny(args, dev, stream, peaks, peak_src):
+    """The exact float32 case (B=H=1, S=128, d=64): launch latency in us."""
+    from online_softmax_attention_rf_gb300 import api
+    w = inputs.WORKLOADS["tiny_fp32"]
+    q_h, k_h, v_h, scale, _ = inputs.workload_inputs("tiny_fp32")
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+    def step():
+        api.attn_fwd(q, k, v, scale, w["causal"], None, o, lse)
+
+    total, per, n = time_side(step, args, stream)
+    assert api.device_status() == 0
+    us = 1000.0 * statistics.median(per)
+    flops = 4.0 * w["d"] * visible_pairs(w)
+    return {"workload": "tiny_fp32 [B=1, H=1, S=128, d=64, f32, non-causal]", "value": us,
+            "unit": "us", "ms_per_step": us / 1000.0, "launches": n,
+            "mean_us": 1000.0 * statistics.mean(per),
+            "gflops": flops / (us * 1e-6) / 1e9,
+            "note": "latency-bound parity case: median CUDA-event time of one launch of the "
+                    "float32 SIMT kernel (inputs resident, 0.13 MB)"}
+
+
+def run_ours(args, dist, rank, world, local):
+    from online_softmax_attention_rf_gb300 import api
+    api.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    side = {"decode": bench_decode, "softmax": bench_softmax,
+            "softmax_long": lambda *a: bench_softmax(*a, name="rows_1m"),
+            "block_sparse": bench_block_sparse, "two_level": bench_two_level,
+            "scattered": bench_scattered, "mla": bench_mla, "cascades": bench_cascades,
+            "tiny": bench_tiny}
+    if args.only in side:
+        # one workload alone (used for profiling captures)
+        out = side[args.only](args, dev, stream, peaks, peak_src)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
+    if args.only == "mha_prefill":
+        out, _ = bench_prefill("mha_prefill", args, dev, stream, peaks, peak_src, args.steps,
+                               args.warmup)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
+
+    # the headline: exactly K timed steps of the GQA long-context prefill
+    clk = ClockSampler(local)
+    head, (q_h, k_h, v_h, scale, w) = bench_prefill(WORKLOAD, args, dev, stream, peaks, peak_src,
+                                                    args.steps, args.warmup, dist, clk)
+    total_ms = max_over_ranks(dist, head["total_ms"])
+    ms_step = total_ms / args.steps
+    flops = head["flops_per_step"]
+    value = flops * world / (ms_step * 1e-3) / 1e12
     if args.only == "prefill":
         if rank == 0:
             print(json.dumps({"workload": WORKLOAD, "value": value, "unit": "TFLOP/s",
-                              "ms_per_step": ms_step, "roofline": roofline}), flush=True)
+                              "ms_per_step": ms_step, "roofline": head["roofline"],
+                              "clocks": clk.summary()}), flush=True)
         return
 
     # end to end through the public API with host buffers: rf_attn_fwd_host
@@ -372,10 +448,18 @@ def run_ours(args, dist, rank, world, local):
     e2e_ms = e2e_total / n_e2e
     h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
     d2h = op.numel() * op.element_size() + lp.numel() * lp.element_size()
-
-    del qp, kp, vp, op, lp, ws
+    del qp, kp, vp, op, lp, ws, q_h, k_h, v_h
     torch.cuda.empty_cache()
 
+    n_mha = max(args.steps, 1)
+    mha, _ = bench_prefill("mha_prefill", args, dev, stream, peaks, peak_src, n_mha, args.warmup)
+    # at least MIN_SIDE_S of launches for the sub-key as well
+    est = mha["ms_per_step"]
+    if n_mha * est < 1000.0 * MIN_SIDE_S:
+        mha, _ = bench_prefill("mha_prefill", args, dev, stream, peaks, peak_src,
+                               int(math.ceil(1000.0 * MIN_SIDE_S / est)), args.warmup)
+    mha.pop("total_ms")
+    tiny = bench_tiny(args, dev, stream, peaks, peak_src)
     decode = bench_decode(args, dev, stream, peaks, peak_src)
     softmax = bench_softmax(args, dev, stream, peaks, peak_src)
     softmax_long = bench_softmax(args, dev, stream, peaks, peak_src, "rows_1m")
@@ -384,25 +468,27 @@ def run_ours(args, dist, rank, world, local):
     scattered = bench_scattered(args, dev, stream, peaks, peak_src)
     mla = bench_mla(args, dev, stream, peaks, peak_src)
     cascades = bench_cascades(args, dev, stream, peaks, peak_src)
-    launches = args.steps
+    launches = args.steps          # one rf_attn_fwd kernel launch per timed step
 
     if rank != 0:
         return
-    cpu_v, cpu_dt, cpu_heads, cores = cpu_oracle_sample(WORKLOAD)
+    cpu_v, cpu_dt, cpu_blocks, cores = cpu_oracle_sample(WORKLOAD)
+    config = workload_config(WORKLOAD, world)
+    config["l2"] = ("inputs larger than L2 (Q, O = 537 MB each per step; K, V = 67 MB each, "
+                    "re-read from L2 by the 8 query heads of a group)")
     line = {
-        "metric": "attn fwd TFLOP/s (prefill); decode GB/s", "value": value, "unit": "TFLOP/s",
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": w["B"], "H": w["H"], "Hkv": w["Hkv"],
-                   "Sq": w["Sq"], "Sk": w["Sk"], "d": w["d"], "causal": w["causal"],
-                   "parallelism": "dp%d (independent replicas)" % world,
-                   "l2": "inputs larger than L2 (Q, K, V, O = 537 MB per step)"},
+        "config": config,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
-        "roofline": roofline,
+        "roofline": head["roofline"],
         "clocks": clk.summary(),
+        "mha_prefill": mha,
+        "tiny_fp32": tiny,
         "decode": decode,
         "softmax": softmax,
         "softmax_long": softmax_long,
@@ -416,10 +502,29 @@ def run_ours(args, dist, rank, world, local):
         "fp8_quant": cascades["fp8_quant"],
         "fp8_gemm": cascades["fp8_gemm"],
         "cpu_baseline": {"value": cpu_v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "%d whole heads of the workload (%.1f s, float64 three-pass "
-                                   "NumPy oracle)" % (cpu_heads, cpu_dt)},
+                         "sample": "%d blocks of 256 query rows of the workload's heads "
+                                   "(%.1f s, float64 three-pass NumPy oracle); TFLOP/s over "
+                                   "the blocks' visible pairs" % (cpu_blocks, cpu_dt)},
     }
     print(json.dumps(line), flush=True)
+
+
+def time_side(fn, args, stream):
+    """Times a secondary workload: at least side_steps(args) launches and at
+    least MIN_SIDE_S seconds of them; returns (total ms, per-launch ms, n)."""
+    for _ in range(args.warmup):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(3):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    est = max(a.elapsed_time(b) / 3.0, 1e-3)
+    n = max(side_steps(args), min(20000, int(math.ceil(1000.0 * MIN_SIDE_S / est))))
+    total, per = time_steps(fn, n, 1, stream, None)
+    return total, per, n
 
 
 def side_steps(args):
@@ -442,7 +547,7 @@ def bench_decode(args, dev, stream, peaks, peak_src):
         api.attn_decode_splitk(q, k, v, w["nsplit"], scale, ws, o, lse)
 
     # K and V (4.3 GB) are far larger than L2: no flush needed
-    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    total, per = time_side(step, args, stream)[:2]
     ms = statistics.mean(per)
     gbs = algo / (ms * 1e-3) / 1e9
     assert api.device_status() == 0
@@ -476,7 +581,7 @@ def bench_block_sparse(args, dev, stream, peaks, peak_src):
         api.attn_fwd(q, k, v, scale, w["causal"], bm, o, lse)
 
     # Q, O (268 MB) exceed L2; K and V of a head (4 MB) are re-read from L2
-    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    total, per = time_side(step, args, stream)[:2]
     ms = statistics.mean(per)
     assert api.device_status() == 0
     tf = flops / (ms * 1e-3) / 1e12
@@ -514,7 +619,7 @@ def bench_scattered(args, dev, stream, peaks, peak_src):
             api.attn_fwd(q, k, v, scale, False, bm, o, lse, kernel=kern)
 
         # Q, K, V, O are 134 MB (above L2); K and V of a head (256 KB) are re-read
-        _, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+        _, per = time_side(step, args, stream)[:2]
         times[kern] = statistics.mean(per)
     assert api.device_status() == 0
     chosen = "row" if choice == api.RF_KERNEL_ROWWISE else "block"
@@ -553,7 +658,7 @@ def bench_mla(args, dev, stream, peaks, peak_src):
         api.mla_decode(q, kv, w["nsplit"], w["scale"], ws, o, lse)
 
     # the latent cache (302 MB) is larger than L2: no flush needed
-    _, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    _, per = time_side(step, args, stream)[:2]
     ms = statistics.mean(per)
     assert api.device_status() == 0
     flops = 2.0 * w["B"] * w["Sk"] * 128 * (576 + 512)
@@ -604,7 +709,7 @@ def bench_two_level(args, dev, stream, peaks, peak_src):
         api.attn_fwd(q, k, v, scale, False, bm, o, lse)
 
     # K and V of a head (4 MB) are re-read from L2 by its CTAs; Q, O (268 MB) exceed L2
-    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    total, per = time_side(step, args, stream)[:2]
     ms = statistics.mean(per)
     assert api.device_status() == 0
     tf = flops / (ms * 1e-3) / 1e12
@@ -634,7 +739,7 @@ def bench_softmax(args, dev, stream, peaks, peak_src, name="rows_64k"):
         api.softmax_rows(x, y)
 
     # x and y (2 GiB) are far larger than L2: no flush needed
-    total, per = time_steps(step, side_steps(args), args.warmup, stream, None)
+    total, per = time_side(step, args, stream)[:2]
     ms = statistics.mean(per)
     gbs = algo / (ms * 1e-3) / 1e9
     assert api.device_status() == 0
@@ -667,7 +772,7 @@ def bench_cascades(args, dev, stream, peaks, peak_src):
                                api._stream())
 
     # logits + outputs = 138 MB per step, larger than L2 (129 MB): no flush
-    total, per = time_steps(step_route, side_steps(args), args.warmup, stream, None)
+    total, per = time_side(step_route, args, stream)[:2]
     ms = statistics.mean(per)
     assert api.device_status() == 0
     gbs = algo / (ms * 1e-3) / 1e9
@@ -692,7 +797,7 @@ def bench_cascades(args, dev, stream, peaks, peak_src):
                                  var.data_ptr(), y.data_ptr(), api.RF_F32, api._stream())
 
     # x and y (1 GiB) are far larger than L2: no flush needed
-    total, per = time_steps(step_moments, side_steps(args), args.warmup, stream, None)
+    total, per = time_side(step_moments, args, stream)[:2]
     ms = statistics.mean(per)
     assert api.device_status() == 0
     gbs = algo / (ms * 1e-3) / 1e9
@@ -717,7 +822,7 @@ def bench_cascades(args, dev, stream, peaks, peak_src):
                                        api._stream())
 
     # points and masses (1.07 GB) are far larger than L2: no flush needed
-    total_ms, per = time_steps(step_inertia, side_steps(args), args.warmup, stream, None)
+    total_ms, per = time_side(step_inertia, args, stream)[:2]
     ms_ = statistics.mean(per)
     assert api.device_status() == 0
     gbs = algo / (ms_ * 1e-3) / 1e9
@@ -748,8 +853,8 @@ def bench_cascades(args, dev, stream, peaks, peak_src):
 
     # A (128 MiB bf16) + codes (64 MiB) exceed L2 for the quantiser; the GEMM
     # reads 128 MiB of codes and writes 128 MiB of C per launch
-    _, per_q = time_steps(step_quant, side_steps(args), args.warmup, stream, None)
-    _, per_g = time_steps(step_gemm, side_steps(args), args.warmup, stream, None)
+    _, per_q = time_side(step_quant, args, stream)[:2]
+    _, per_g = time_side(step_gemm, args, stream)[:2]
     assert api.device_status() == 0
     ms_q, ms_g = statistics.mean(per_q), statistics.mean(per_g)
     qbytes = a.numel() * 2 + qa.numel() + sa.numel() * 4
@@ -780,12 +885,12 @@ def bench_cascades(args, dev, stream, peaks, peak_src):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "softmax", "softmax_long",
-                                       "block_sparse", "two_level", "scattered", "mla",
-                                       "cascades"],
+    ap.add_argument("--only", choices=["all", "prefill", "mha_prefill", "tiny", "decode",
+                                       "softmax", "softmax_long", "block_sparse", "two_level",
+                                       "scattered", "mla", "cascades"],
                     default="all",
                     help="time one workload alone (for profiling); the default runs all")
     args = ap.parse_args()

@@ -208,14 +208,21 @@ rf_status rf_attn_decode_splitk(const void *q, const void *k, const void *v, voi
  * call).
  *  - Sizes whose workspace, rf_decode_workspace_bytes(B,H,nsplit,d), exceeds
  *    16 MiB (16777216 bytes) are rejected with RF_ERR_INVALID.
+ *  - Invalid arguments are rejected as by rf_attn_decode_splitk, before any
+ *    CUDA call.
  *  - The first call on a device looks up the array's device address on that
- *    device (cudaGetSymbolAddress); make that first call before any stream
- *    capture.
+ *    device (cudaGetSymbolAddress) and caches it for the current context;
+ *    after cudaDeviceReset, or when the device's context is created again,
+ *    the next call looks it up again. Make the first call in a context
+ *    before any stream capture.
  *  - Every call on a device shares the one array, which keeps the previous
- *    call's partials; each call writes every partial before reading it, so
- *    nothing needs clearing, but calls that overlap on the GPU (different
+ *    call's partials. A successful call writes every partial before reading
+ *    it, so nothing needs clearing; calls that overlap on the GPU (different
  *    streams, or concurrent host threads) race on it and must be serialised
  *    by the caller.
+ *  - When rf_device_status reports RF_ERR_TIMEOUT after a call, a partials
+ *    CTA gave up before writing its split, and that call's O and LSE are
+ *    undefined (they may combine an earlier call's partials).
  */
 rf_status rf_attn_decode_splitk_noalloc(const void *q, const void *k, const void *v, void *o,
                                         float *lse, int B, int H, int Hkv, int Sk, int d,

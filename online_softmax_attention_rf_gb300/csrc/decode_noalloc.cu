@@ -11,9 +11,11 @@
 // exactly the allocating entry point's kernels on it.
 //
 // The array's name, used in host code, stands for a host-side shadow, not a
-// device address, so the device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached.
-#include <atomic>
+// device address. The device address is looked up with cudaGetSymbolAddress
+// (with the device current) and cached per device, tagged with the current
+// context's unique id: after cudaDeviceReset, or once the primary context has
+// been released and created again, the module is loaded anew and the array
+// may sit elsewhere, so a changed id forces a new lookup.
 #include <cstdio>
 
 #include "rf_internal.h"
@@ -26,23 +28,7 @@ constexpr size_t kScratchBytes = size_t(16) << 20;
 
 __device__ __align__(256) float g_decode_scratch[kScratchBytes / sizeof(float)];
 
-std::atomic<float*> g_scratch_addr[128];
-
-// Device address of the array on the current device, looked up on first use.
-float* scratch_address(cudaError_t* err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev >= 0 && dev < 128) {
-    float* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p != nullptr) return p;
-  }
-  float* p = nullptr;
-  *err = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_decode_scratch);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev >= 0 && dev < 128) g_scratch_addr[dev].store(p, std::memory_order_release);
-  return p;
-}
+rf::SymbolCache g_scratch_cache;
 
 }  // namespace
 
@@ -50,6 +36,10 @@ extern "C" rf_status rf_attn_decode_splitk_noalloc(const void* q, const void* k,
                                                    void* o, float* lse, int B, int H, int Hkv,
                                                    int Sk, int d, float scale, int nsplit,
                                                    rf_dtype dt, rf_stream stream) {
+  // every argument is checked on the host before any CUDA call
+  const rf_status chk = rf::check_decode_args("rf_attn_decode_splitk_noalloc", q, k, v, o, lse,
+                                              B, H, Hkv, Sk, d, scale, nsplit, dt);
+  if (chk != RF_OK) return chk;
   const size_t need = rf_decode_workspace_bytes(B, H, nsplit, d);
   if (need > kScratchBytes) {
     char msg[200];
@@ -60,15 +50,18 @@ extern "C" rf_status rf_attn_decode_splitk_noalloc(const void* q, const void* k,
     return rf::set_last_error(RF_ERR_INVALID, msg);
   }
   cudaError_t e = cudaSuccess;
-  float* ws = scratch_address(&e);
+  float* ws = static_cast<float*>(rf::symbol_address(g_decode_scratch, g_scratch_cache, &e));
   if (ws == nullptr) {
     char msg[200];
     snprintf(msg, sizeof(msg), "rf_attn_decode_splitk_noalloc: static workspace lookup: %s",
              cudaGetErrorString(e));
     return rf::set_last_error(RF_ERR_CUDA, msg);
   }
-  // every partial the kernels read is written by them first in the same call,
-  // so nothing in the array needs clearing between calls
+  // On success every partial the merge reads was written earlier in the same
+  // call, so the array needs no clearing between calls. A partials CTA that
+  // gives up on a timed-out wait returns without writing its split; O and LSE
+  // are then undefined (they may mix in an earlier call's partials) and
+  // rf_device_status reports RF_ERR_TIMEOUT.
   return rf_attn_decode_splitk(q, k, v, o, lse, B, H, Hkv, Sk, d, scale, nsplit, ws, kScratchBytes,
                                dt, stream);
 }

@@ -21,7 +21,46 @@ thread_local int g_fault_site = 0;
 
 // The device status word (one per device that loads the library).
 __device__ int g_status_word = 0;
-std::atomic<int*> g_status_ptr[128];
+rf::SymbolCache g_status_cache;
+
+// Driver calls that identify the current context, looked up once through the
+// runtime (the library links no driver import). Null when unavailable.
+using CtxGetCurrentFn = int (*)(void** ctx);
+using CtxGetIdFn = int (*)(void* ctx, unsigned long long* id);
+
+struct CtxFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const CtxFns& ctx_fns() {
+  static const CtxFns fns = [] {
+    CtxFns f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<CtxGetIdFn>(p);
+    return f;
+  }();
+  return fns;
+}
+
+// Unique id of the calling thread's current context; 0 when there is none
+// or it cannot be read (then nothing is cached).
+unsigned long long current_ctx_id() {
+  const CtxFns& f = ctx_fns();
+  if (f.get_current == nullptr || f.get_id == nullptr) return 0;
+  void* ctx = nullptr;
+  if (f.get_current(&ctx) != 0 || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (f.get_id(ctx, &id) != 0) return 0;
+  return id;
+}
 
 rf_status fail(rf_status st, const char* fmt, ...) {
   va_list ap;
@@ -48,20 +87,57 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 namespace rf {
 
-int* status_word() {
+void* symbol_address(const void* symbol, SymbolCache& cache, cudaError_t* err) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  if (dev >= 0 && dev < 128) {
-    int* p = g_status_ptr[dev].load(std::memory_order_acquire);
-    if (p != nullptr) return p;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  const bool slot = dev >= 0 && dev < 128;
+  unsigned long long id = current_ctx_id();
+  if (slot && id != 0) {
+    std::lock_guard<std::mutex> g(cache.mu);
+    if (cache.ctx_id[dev] == id && cache.ptr[dev] != nullptr) return cache.ptr[dev];
   }
   void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-  if (dev >= 0 && dev < 128) g_status_ptr[dev].store(static_cast<int*>(p), std::memory_order_release);
-  return static_cast<int*>(p);
+  *err = cudaGetSymbolAddress(&p, symbol);
+  if (*err != cudaSuccess) return nullptr;
+  id = current_ctx_id();  // the lookup may have made the primary context current
+  if (slot && id != 0) {
+    std::lock_guard<std::mutex> g(cache.mu);
+    cache.ctx_id[dev] = id;
+    cache.ptr[dev] = p;
+  }
+  return p;
+}
+
+int* status_word() {
+  cudaError_t e = cudaSuccess;
+  return static_cast<int*>(symbol_address(&g_status_word, g_status_cache, &e));
 }
 
 rf_status set_last_error(rf_status st, const char* msg) { return fail(st, "%s", msg); }
+
+rf_status check_decode_args(const char* who, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, int B, int H, int Hkv, int Sk,
+                            int d, float scale, int nsplit, rf_dtype dt) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sk < 1 || d < 1) return fail(RF_ERR_INVALID, "%s: bad sizes", who);
+  if (H % Hkv != 0) return fail(RF_ERR_INVALID, "%s: H %% Hkv != 0", who);
+  if (H / Hkv > 16) return fail(RF_ERR_UNSUPPORTED, "%s: H/Hkv > 16", who);
+  if (nsplit < 1 || nsplit > Sk) return fail(RF_ERR_INVALID, "%s: need 1 <= nsplit <= Sk", who);
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(RF_ERR_INVALID, "%s: scale must be finite and > 0", who);
+  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "%s: dtype", who);
+  if (dt != RF_BF16 || (d != 64 && d != 128))
+    return fail(RF_ERR_UNSUPPORTED, "%s: bf16 with d in {64,128} only", who);
+  if (int64_t(B) * Hkv * Sk * d * 2 > (int64_t(1) << 46))
+    return fail(RF_ERR_INVALID, "%s: tensors too large", who);
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr)
+    return fail(RF_ERR_INVALID, "%s: NULL pointer", who);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(RF_ERR_INVALID, "%s: pointers must be 16-byte aligned", who);
+  if (lse != nullptr && !aligned(lse, 4))
+    return fail(RF_ERR_INVALID, "%s: lse must be 4-byte aligned", who);
+  return RF_OK;
+}
 
 uint8_t* debug_visited(int64_t* len) {
   if (len != nullptr) *len = g_visited_len;
@@ -251,26 +327,12 @@ size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d) {
 rf_status rf_attn_decode_splitk(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int B, int H, int Hkv, int Sk, int d, float scale, int nsplit,
                                 float* ws, size_t ws_bytes, rf_dtype dt, rf_stream stream) {
-  if (B < 1 || H < 1 || Hkv < 1 || Sk < 1 || d < 1)
-    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: bad sizes");
-  if (H % Hkv != 0) return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: H %% Hkv != 0");
-  if (H / Hkv > 16) return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitk: H/Hkv > 16");
-  if (nsplit < 1 || nsplit > Sk)
-    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: need 1 <= nsplit <= Sk");
-  if (!(scale > 0.f) || !std::isfinite(scale))
-    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: scale must be finite and > 0");
-  if (dt != RF_F32 && dt != RF_BF16) return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: dtype");
-  if (dt != RF_BF16 || (d != 64 && d != 128))
-    return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitk: bf16 with d in {64,128} only");
-  if (int64_t(B) * Hkv * Sk * d * 2 > (int64_t(1) << 46))
-    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: tensors too large");
-  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || ws == nullptr)
-    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: NULL pointer");
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      !aligned(ws, 16))
+  const rf_status chk = rf::check_decode_args("rf_attn_decode_splitk", q, k, v, o, lse, B, H, Hkv,
+                                              Sk, d, scale, nsplit, dt);
+  if (chk != RF_OK) return chk;
+  if (ws == nullptr) return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: NULL pointer");
+  if (!aligned(ws, 16))
     return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: pointers must be 16-byte aligned");
-  if (lse != nullptr && !aligned(lse, 4))
-    return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: lse must be 4-byte aligned");
   if (ws_bytes < rf_decode_workspace_bytes(B, H, nsplit, d))
     return fail(RF_ERR_INVALID, "rf_attn_decode_splitk: workspace too small (%zu < %zu)",
                 ws_bytes, rf_decode_workspace_bytes(B, H, nsplit, d));

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "rf.h"
 
 // Upper bound on any single device-side wait (mbarrier phase, TMEM, peer).
@@ -34,6 +36,31 @@ __host__ __device__ constexpr int dev_code(int kind, int kernel, int site) {
 
 // Device address of the status word for the current device (nullptr on error).
 int* status_word();
+
+// Device addresses of one __device__ variable, one per device, each tagged
+// with the unique id of the context it was looked up in. A context that was
+// torn down and created again (cudaDeviceReset, a primary context released
+// and retained) gets a new id and may hold the variable at another address,
+// so a tag that no longer matches the current context forces a new lookup.
+struct SymbolCache {
+  std::mutex mu;
+  unsigned long long ctx_id[128] = {};
+  void* ptr[128] = {};
+};
+
+// Device address of `symbol` (the host-side name of a __device__ variable of
+// this library) in the calling thread's current context: the cached address
+// when the context's id matches, else cudaGetSymbolAddress (which makes the
+// device's primary context current if none is). Returns nullptr and sets
+// *err on failure.
+void* symbol_address(const void* symbol, SymbolCache& cache, cudaError_t* err);
+
+// Host-side checks shared by rf_attn_decode_splitk and its allocation-free
+// variant: everything but the workspace. `who` names the entry point in the
+// message. Makes no CUDA call.
+rf_status check_decode_args(const char* who, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, int B, int H, int Hkv, int Sk,
+                            int d, float scale, int nsplit, rf_dtype dt);
 
 // Sets this thread's rf_last_error() message and returns st.
 rf_status set_last_error(rf_status st, const char* msg);

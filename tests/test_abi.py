@@ -124,6 +124,36 @@ def test_decode_rejects(L, kw, expect):
     assert _decode(L, **kw) == expect
 
 
+def _decode_noalloc(L, q=A, k=A, v=A, o=A, lse=A, B=2, H=8, Hkv=2, Sk=1000, d=128, scale=0.1,
+                    nsplit=4, dt=api.RF_BF16):
+    return L.rf_attn_decode_splitk_noalloc(q, k, v, o, lse, B, H, Hkv, Sk, d, scale, nsplit, dt,
+                                           None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), api.RF_ERR_INVALID),
+    (dict(k=None), api.RF_ERR_INVALID),
+    (dict(v=None), api.RF_ERR_INVALID),
+    (dict(o=None), api.RF_ERR_INVALID),
+    (dict(q=MIS), api.RF_ERR_INVALID),
+    (dict(lse=A + 2), api.RF_ERR_INVALID),
+    (dict(Hkv=3), api.RF_ERR_INVALID),               # H % Hkv
+    (dict(nsplit=0), api.RF_ERR_INVALID),
+    (dict(nsplit=1001), api.RF_ERR_INVALID),         # more splits than keys
+    (dict(B=0), api.RF_ERR_INVALID),                 # would need no workspace at all
+    (dict(scale=math.nan), api.RF_ERR_INVALID),
+    (dict(dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
+    (dict(d=96), api.RF_ERR_UNSUPPORTED),
+    (dict(H=64, Hkv=2), api.RF_ERR_UNSUPPORTED),
+    # partials of 64 x 32 rows x 64 splits x 129 floats: 67.6 MB > the 16 MiB array
+    (dict(B=64, H=32, Hkv=8, Sk=65536, nsplit=64), api.RF_ERR_INVALID),
+])
+def test_decode_noalloc_rejects_before_any_cuda_call(L, kw, expect):
+    # on a machine without a GPU any CUDA call would give RF_ERR_CUDA instead
+    assert _decode_noalloc(L, **kw) == expect
+    assert L.rf_last_error().decode().startswith("rf_attn_decode_splitk_noalloc")
+
+
 @pytest.mark.parametrize("args,expect", [
     ((A, A, A, A, 5, 0, 64, api.RF_BF16), api.RF_ERR_INVALID),      # nsplit 0
     ((A, A, A, A, 5, 4, 2048, api.RF_BF16), api.RF_ERR_INVALID),    # d > 1024

@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _tols(dtype):
-    return (TOL_F32, TOL_F32 * 100) if dtype == "f32" else (TOL_BF16_O, TOL_BF16_LSE)
+    return (TOL_F32, TOL_F32) if dtype == "f32" else (TOL_BF16_O, TOL_BF16_LSE)
 
 
 def _compare(B, H, Hkv, Sq, Sk, d, causal, dtype, seed, tile_mask=None, elem_mask=None):

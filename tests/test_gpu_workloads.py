@@ -107,3 +107,48 @@ def test_softmax_rows_sampled(cuda_device, name):
     # every row sums to one (a property at any size)
     s = y.double().sum(dim=1)
     assert torch.allclose(s, torch.ones_like(s), atol=1e-4)
+
+
+def _visited_full(name, make_blockmask, want_tiles):
+    """Runs a full-size workload exactly as bench.py launches it, recording
+    the tiles each query tile's MMA issuer visits, and compares all heads
+    with the oracle's set of tiles holding a visible pair (STOF,
+    Méthodologie: masked tiles are skipped entirely)."""
+    w = inputs.WORKLOADS[name]
+    q, k, v, scale, extras = inputs.workload_inputs(name)
+    nqt, nkt = inputs.n_tiles(w["Sq"]), inputs.n_tiles(w["Sk"])
+    nheads = w["B"] * w["H"]
+    buf = torch.zeros(nheads * nqt * nkt, dtype=torch.uint8, device="cuda")
+    bm = make_blockmask(extras)
+    api.set_debug_visited(buf)
+    try:
+        api.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale, w["causal"], bm)
+        assert api.device_status() == 0
+    finally:
+        api.set_debug_visited(None)
+    got = buf.cpu().numpy().reshape(nheads, nqt, nkt).astype(bool)
+    want = want_tiles(w, extras)
+    for n in range(nheads):
+        bad = np.argwhere(got[n] != want)
+        assert bad.size == 0, "%s head %d: %d tiles differ, first %s" % (
+            name, n, len(bad), bad[:5].tolist())
+    return want
+
+
+def test_block_sparse_skip_set_full_size(cuda_device):
+    want = _visited_full(
+        "block_sparse", lambda ex: api.BlockMask.from_dense(ex["tile_mask"]),
+        lambda w, ex: oracle.visited_tiles(w["Sq"], w["Sk"], w["causal"], ex["tile_mask"], 128))
+    assert int(want.sum()) == 1722           # the workload's tile count per head
+
+
+def test_two_level_skip_set_full_size(cuda_device):
+    want = _visited_full(
+        "two_level", lambda ex: api.BlockMask.from_dense_elements(ex["elem_mask"]),
+        lambda w, ex: oracle.visited_tiles(w["Sq"], w["Sk"], w["causal"],
+                                           elem_mask=ex["elem_mask"]))
+    # the visited set is exactly the set of listed tiles of the encoding
+    w = inputs.WORKLOADS["two_level"]
+    rp, _, _, _ = oracle.two_level_encode(inputs.band_global_mask(w["Sq"], w["band"],
+                                                                  w["n_global"]))
+    assert int(want.sum()) == int(rp[-1])
