@@ -49,6 +49,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch from ncu captures (summarised under profiles/), valid only for the
 # kernel source they were taken on; any change to the source makes it null.
 TRAFFIC = {
+    # attn_tc_kernel<128, 0> on gqa_long: dram read 677.3 MB + write 505.0 MB
+    "attn_tc_gqa_long": {"digest": "8dc32d453b50a32d", "bytes": 1182318592,
+                         "sources": ("attn_tc.cu", "rf_device.cuh")},
     # attn_tc_kernel<128, 0> on mha_prefill: dram read 404.2 MB + write 113.1 MB
     "attn_tc_mha_prefill": {"digest": "8dc32d453b50a32d", "bytes": 517277696,
                             "sources": ("attn_tc.cu", "rf_device.cuh")},
@@ -455,9 +458,9 @@ def run_ours(args, dist, rank, world, local):
     mha, _ = bench_prefill("mha_prefill", args, dev, stream, peaks, peak_src, n_mha, args.warmup)
     # at least MIN_SIDE_S of launches for the sub-key as well
     est = mha["ms_per_step"]
-    if n_mha * est < 1000.0 * MIN_SIDE_S:
+    if n_mha * est < 1000.0 * args.min_side_s:
         mha, _ = bench_prefill("mha_prefill", args, dev, stream, peaks, peak_src,
-                               int(math.ceil(1000.0 * MIN_SIDE_S / est)), args.warmup)
+                               int(math.ceil(1000.0 * args.min_side_s / est)), args.warmup)
     mha.pop("total_ms")
     tiny = bench_tiny(args, dev, stream, peaks, peak_src)
     decode = bench_decode(args, dev, stream, peaks, peak_src)
@@ -511,7 +514,7 @@ def run_ours(args, dist, rank, world, local):
 
 def time_side(fn, args, stream):
     """Times a secondary workload: at least side_steps(args) launches and at
-    least MIN_SIDE_S seconds of them; returns (total ms, per-launch ms, n)."""
+    least args.min_side_s seconds of them; returns (total ms, per-launch ms, n)."""
     for _ in range(args.warmup):
         fn()
     a = torch.cuda.Event(enable_timing=True)
@@ -522,7 +525,7 @@ def time_side(fn, args, stream):
     b.record(stream)
     b.synchronize()
     est = max(a.elapsed_time(b) / 3.0, 1e-3)
-    n = max(side_steps(args), min(20000, int(math.ceil(1000.0 * MIN_SIDE_S / est))))
+    n = max(side_steps(args), min(20000, int(math.ceil(1000.0 * args.min_side_s / est))))
     total, per = time_steps(fn, n, 1, stream, None)
     return total, per, n
 
@@ -888,6 +891,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--min-side-s", type=float, default=MIN_SIDE_S,
+                    help="least time over which each secondary workload is timed (a launch "
+                         "list capture sets 0: a few launches of each)")
     ap.add_argument("--only", choices=["all", "prefill", "mha_prefill", "tiny", "decode",
                                        "softmax", "softmax_long", "block_sparse", "two_level",
                                        "scattered", "mla", "cascades"],
