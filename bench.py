@@ -611,7 +611,7 @@ def bench_scattered(args, dev, stream, peaks, peak_src):
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     bm = api.BlockMask.from_dense_elements(em, device=dev)
-    counts = api.selector_counts(w["B"], w["H"], w["Sq"], w["Sk"], False, bm)
+    counts = api.selector_counts(w["B"], w["H"], w["Sq"], w["Sk"], False, bm, dev)
     choice = api.choose_kernel(w["B"], w["H"], w["Sq"], w["Sk"], w["d"], *counts, device=dev)
     est_block, est_row = api.estimate_us(w["B"], w["H"], w["Sq"], w["Sk"], w["d"], *counts,
                                          device=dev)

@@ -228,6 +228,21 @@ rf_status rf_attn_decode_splitk_noalloc(const void *q, const void *k, const void
                                         float *lse, int B, int H, int Hkv, int Sk, int d,
                                         float scale, int nsplit, rf_dtype dt, rf_stream stream);
 
+/*
+ * The partials step of rf_attn_decode_splitk alone (multi-segment strategy,
+ * RedFuser section 3: the per-segment results before the merge). Writes into
+ * ws, laid out as rf_attn_decode_splitk's workspace,
+ *   o_part float32 [B*H, nsplit, d] (each split's O, normalised within it),
+ *   then lse_part float32 [B*H, nsplit] (natural log; -inf for no key),
+ * and launches nothing else. A rank holding a contiguous shard of the keys
+ * computes its partials with this call, merges them (rf_splitk_merge with
+ * out_dt RF_F32), exchanges the per-rank results and merges those with
+ * rf_splitk_merge_strided. Arguments and errors as rf_attn_decode_splitk.
+ */
+rf_status rf_attn_decode_partials(const void *q, const void *k, const void *v, float *ws,
+                                  size_t ws_bytes, int B, int H, int Hkv, int Sk, int d,
+                                  float scale, int nsplit, rf_dtype dt, rf_stream stream);
+
 /* Bytes of workspace rf_attn_decode_splitk needs: 4 * B*H*nsplit*(d + 1),
  * rounded up to 256. Returns 0 for non-positive arguments. */
 size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d);
@@ -243,6 +258,23 @@ size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d);
 rf_status rf_splitk_merge(const float *o_part, const float *lse_part, void *o, float *lse,
                           int64_t rows, int nsplit, int d, rf_dtype out_dt,
                           rf_stream stream);
+
+/*
+ * The same merge over partials laid out with explicit element strides:
+ * partial s of row r is the d floats at o_part + s * o_split_stride +
+ * r * o_row_stride, with its lse at lse_part[s * lse_split_stride +
+ * r * lse_row_stride]. rf_splitk_merge is the row-major case
+ * (o strides d and nsplit * d, lse strides 1 and nsplit). The split-major
+ * case [nsplit, rows, d] (o strides rows * d and d, lse strides rows and 1)
+ * is what an all-gather of per-rank partials produces when the keys are
+ * sharded across GPUs (RedFuser, section 3, multi-segment strategy:
+ * partition the input, then merge the partial results), so it is merged
+ * without a transposing copy. Strides >= 0; other rules as rf_splitk_merge.
+ */
+rf_status rf_splitk_merge_strided(const float *o_part, const float *lse_part, void *o, float *lse,
+                                  int64_t rows, int nsplit, int d, int64_t o_split_stride,
+                                  int64_t o_row_stride, int64_t lse_split_stride,
+                                  int64_t lse_row_stride, rf_dtype out_dt, rf_stream stream);
 
 /*
  * Build block-sparse tile lists from a dense tile mask on the device.
@@ -299,6 +331,27 @@ rf_status rf_attn_fwd_rowwise(const void *q, const void *k, const void *v, void 
                               int B, int H, int Hkv, int Sq, int Sk, int d, float scale,
                               int causal, const rf_blockmask *blockmask, rf_dtype dt,
                               rf_stream stream);
+
+/*
+ * Inputs of the kernel selector below, counted on the device from the tile
+ * lists themselves (STOF, Méthodologie, unified MHA module: the selection is
+ * taken from the mask's sparsity, which the lists already encode).
+ *  bm     : the lists as rf_attn_fwd takes them (NULL: dense), for an
+ *           attention of B x H heads, Sq queries, Sk keys, causal 0/1.
+ *  counts : device int64[3], caller-owned, overwritten on the stream with
+ *           counts[0] = listed tiles that hold a visible pair (tiles the
+ *                       attention kernels process), over all B*H heads;
+ *           counts[1] = how many of them are partial (two-level masks);
+ *           counts[2] = visible (query, key) pairs over all heads, after the
+ *                       causal limit and the inner bitmaps.
+ *           A list shared by all heads (per_head 0) counts once per head.
+ * Asynchronous: read counts after the stream has reached the call. Out-of-
+ * range tile indices are skipped and reported through rf_device_status.
+ * Errors: RF_ERR_INVALID (bad sizes or list fields, counts NULL or not
+ * 8-byte aligned), RF_ERR_CUDA.
+ */
+rf_status rf_blockmask_counts(const rf_blockmask *bm, int B, int H, int Sq, int Sk, int causal,
+                              int64_t *counts, rf_stream stream);
 
 #define RF_KERNEL_BLOCKWISE 0  /* rf_attn_fwd */
 #define RF_KERNEL_ROWWISE 1    /* rf_attn_fwd_rowwise */

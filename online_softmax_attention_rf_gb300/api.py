@@ -12,7 +12,6 @@ import ctypes
 import math
 import os
 
-import numpy as np
 import torch
 
 from . import build as _build
@@ -60,8 +59,13 @@ SIGNATURES = {
     "rf_attn_fwd_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "rf_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "rf_splitk_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P]),
+    "rf_attn_decode_partials": (_I, [_P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _F,
+                                     _I, _I, _P]),
+    "rf_splitk_merge_strided": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I64, _I64, _I64, _I64, _I,
+                                     _P]),
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
     "rf_blockmask_build_elements": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
+    "rf_blockmask_counts": (_I, [ctypes.POINTER(RFBlockMask), _I, _I, _I, _I, _I, _P, _P]),
     "rf_attn_fwd_rowwise": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
                                  ctypes.POINTER(RFBlockMask), _I, _P]),
     "rf_attn_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I64, _I64, _I64, _I]),
@@ -144,14 +148,10 @@ class BlockMask:
     tile) and ``bits`` uint64 viewed as int64 [partial tiles, 256].
     """
 
-    def __init__(self, row_ptr, col_idx, nqt, nkt, per_head, tile_bits=None, bits=None,
-                 host_mask=None):
+    def __init__(self, row_ptr, col_idx, nqt, nkt, per_head, tile_bits=None, bits=None):
         self.row_ptr, self.col_idx = row_ptr, col_idx
         self.nqt, self.nkt, self.per_head = nqt, nkt, per_head
         self.tile_bits, self.bits = tile_bits, bits
-        # host copy of the mask it was built from (tile or element level),
-        # for the kernel selector's counts; None when built from lists
-        self.host_mask = host_mask
 
     def as_struct(self):
         return RFBlockMask(TILE, TILE, self.nqt, self.nkt, self.row_ptr.data_ptr(),
@@ -179,8 +179,7 @@ class BlockMask:
         blockmask_build_elements(dense, row_ptr, col_idx, tile_bits, None, n_partial)
         bits = torch.empty((max(1, int(n_partial.item())), 256), dtype=torch.int64, device=device)
         blockmask_build_elements(dense, row_ptr, col_idx, tile_bits, bits, n_partial)
-        return cls(row_ptr, col_idx, nqt, nkt, per_head, tile_bits, bits,
-                   host_mask=("elements", em.cpu().numpy().astype(bool)))
+        return cls(row_ptr, col_idx, nqt, nkt, per_head, tile_bits, bits)
 
     @classmethod
     def from_dense(cls, tile_mask, device="cuda"):
@@ -195,8 +194,7 @@ class BlockMask:
         row_ptr = torch.empty(nheads * nqt + 1, dtype=torch.int32, device=device)
         col_idx = torch.empty(max(1, nheads * nqt * nkt), dtype=torch.int32, device=device)
         blockmask_build(dense, row_ptr, col_idx)
-        return cls(row_ptr, col_idx, nqt, nkt, per_head,
-                   host_mask=("tiles", tm.cpu().numpy().astype(bool)))
+        return cls(row_ptr, col_idx, nqt, nkt, per_head)
 
 
 def blockmask_build(dense_u8, row_ptr, col_idx):
@@ -336,7 +334,7 @@ def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=No
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if kernel == "auto":
-        counts = selector_counts(B, H, Sq, Sk, causal, blockmask)
+        counts = selector_counts(B, H, Sq, Sk, causal, blockmask, q.device)
         kernel = "row" if choose_kernel(B, H, Sq, Sk, d, *counts, device=q.device) == \
             RF_KERNEL_ROWWISE else "block"
     if kernel not in ("block", "row"):
@@ -389,39 +387,19 @@ def _num_sms(device):
     return 152
 
 
-def selector_counts(B, H, Sq, Sk, causal, blockmask=None):
-    """(listed_tiles, partial_tiles, visible_pairs) over all B*H heads: the
-    selector's inputs, counted on the host from the mask a BlockMask was built
-    from (dense when blockmask is None)."""
-    nqt, nkt = -(-Sq // TILE), -(-Sk // TILE)
-    rows = np.arange(Sq)[:, None]
-    cols = np.arange(Sk)[None, :]
-    vis = (cols <= rows + (Sk - Sq)) if causal else np.ones((Sq, Sk), dtype=bool)
-    heads = B * H
-    kind, m = ("dense", None) if blockmask is None else (blockmask.host_mask or (None, None))
-    if kind is None:
-        raise ValueError("this BlockMask keeps no host mask; pass the counts yourself")
-    if kind == "dense":
-        em = vis[None]
-    elif kind == "tiles":
-        em = np.repeat(np.repeat(m, TILE, axis=-2), TILE, axis=-1)[..., :Sq, :Sk] & vis
-    else:
-        em = m & vis
-
-    def per_tile(x):
-        pad = np.zeros((x.shape[0], nqt * TILE, nkt * TILE), dtype=bool)
-        pad[:, :Sq, :Sk] = x
-        return pad.reshape(x.shape[0], nqt, TILE, nkt, TILE).sum(axis=(2, 4))
-
-    listed = per_tile(em) > 0
-    if kind == "elements":
-        # partial in the two-level encoding (the causal limit costs nothing extra)
-        inside = np.ones((1, Sq, Sk), dtype=bool)
-        partial = listed & (per_tile(m) < per_tile(inside))
-    else:
-        partial = np.zeros_like(listed)
-    scale = heads if em.shape[0] == 1 else 1
-    return (int(listed.sum()) * scale, int(partial.sum()) * scale, int(em.sum()) * scale)
+def selector_counts(B, H, Sq, Sk, causal, blockmask=None, device=None):
+    """rf_blockmask_counts: (listed_tiles, partial_tiles, visible_pairs) over
+    all B*H heads, the selector's inputs, counted on the device from the tile
+    lists (dense when blockmask is None); waits for the three numbers."""
+    dev = blockmask.row_ptr.device if blockmask is not None else (
+        torch.device("cuda", torch.cuda.current_device()) if device is None else device)
+    counts = torch.empty(3, dtype=torch.int64, device=dev)
+    bm = ctypes.byref(blockmask.as_struct()) if blockmask is not None else None
+    with torch.cuda.device(dev):
+        _check(lib().rf_blockmask_counts(bm, B, H, Sq, Sk, 1 if causal else 0, _ptr(counts),
+                                         _stream()))
+        listed, partial, pairs = (int(x) for x in counts.cpu().tolist())
+    return listed, partial, pairs
 
 
 def attn_fwd_host_workspace_bytes(B, H, Hkv, Sq, Sk, d, dtype=torch.bfloat16):
@@ -502,14 +480,50 @@ def attn_decode_splitk_noalloc(q, k, v, nsplit, scale=None, out=None, lse=None):
     return o, lse
 
 
+def attn_decode_partials(q, k, v, nsplit, scale=None, workspace=None):
+    """rf_attn_decode_partials: q [B,H,1,d], k/v [B,Hkv,Sk,d] bf16 -> (o_part
+    float32 [B*H, nsplit, d], lse_part float32 [B*H, nsplit]), views of the
+    workspace."""
+    _cuda(q, k, v)
+    B, H, _, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nbytes = decode_workspace_bytes(B, H, nsplit, d)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device) \
+        if workspace is None else workspace
+    _cuda(ws)
+    _check(lib().rf_attn_decode_partials(_ptr(q), _ptr(k), _ptr(v), _ptr(ws),
+                                         ws.numel() * ws.element_size(), B, H, Hkv, Sk, d,
+                                         float(scale), int(nsplit), _dt(q), _stream()))
+    n = B * H * nsplit
+    return ws[:n * d].view(B * H, nsplit, d), ws[n * d:n * d + n].view(B * H, nsplit)
+
+
 def splitk_merge(o_part, lse_part, out_dtype=torch.bfloat16):
-    """rf_splitk_merge: o_part [rows, nsplit, d] f32, lse_part [rows, nsplit] f32."""
-    _cuda(o_part, lse_part)
+    """rf_splitk_merge: o_part [rows, nsplit, d] f32, lse_part [rows, nsplit] f32.
+
+    Contiguous partials go to rf_splitk_merge; strided views (for instance
+    ``gathered.permute(1, 0, 2)`` of split-major [nsplit, rows, d] partials,
+    with d contiguous) go to rf_splitk_merge_strided with their strides."""
+    for t in (o_part, lse_part):
+        if not t.is_cuda or t.dtype != torch.float32:
+            raise ValueError("partials must be float32 CUDA tensors")
     rows, nsplit, d = o_part.shape
+    if lse_part.shape != (rows, nsplit):
+        raise ValueError("lse_part must be [rows, nsplit]")
     o = torch.empty(rows, d, dtype=out_dtype, device=o_part.device)
     lse = torch.empty(rows, dtype=torch.float32, device=o_part.device)
-    _check(lib().rf_splitk_merge(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), rows, nsplit,
-                                 d, RF_F32 if out_dtype == torch.float32 else RF_BF16, _stream()))
+    out_dt = RF_F32 if out_dtype == torch.float32 else RF_BF16
+    if o_part.is_contiguous() and lse_part.is_contiguous():
+        _check(lib().rf_splitk_merge(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), rows,
+                                     nsplit, d, out_dt, _stream()))
+    else:
+        if o_part.stride(2) != 1:
+            raise ValueError("o_part's last dimension must be contiguous")
+        _check(lib().rf_splitk_merge_strided(
+            _ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), rows, nsplit, d, o_part.stride(1),
+            o_part.stride(0), lse_part.stride(1), lse_part.stride(0), out_dt, _stream()))
     return o, lse
 
 

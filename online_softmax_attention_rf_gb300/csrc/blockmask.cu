@@ -253,6 +253,107 @@ __global__ void __launch_bounds__(256) tile_bits_kernel(const uint8_t* __restric
 
 }  // namespace
 
+// Inputs of the analytic kernel selector, counted over the tile lists the
+// attention kernels walk (STOF, Méthodologie, unified MHA module: the choice
+// between the row-wise and block-wise kernels is taken from the sparsity).
+// One CTA per list row (a query tile of a head); warp w takes the row's
+// entries w, w + 8, ... For each entry it counts the visible (query, key)
+// pairs of the tile: a full tile by the closed form of each row's causal
+// limit, a partial tile (two-level mask) as the popcount of its 256 inner
+// 8 x 8 words with the causal limit applied bit-wise. An entry is counted as
+// listed when it holds a visible pair (the attention kernels skip the others),
+// and as partial when it is also partial in the encoding. Without lists the
+// row is the dense or causal range of key tiles. Counts of a list shared by
+// all heads (or of no list) are multiplied by `mult` = B * H.
+__global__ void __launch_bounds__(256) blockmask_counts_kernel(
+    const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx,
+    const int32_t* __restrict__ tile_bits, const uint64_t* __restrict__ bits, int nqt, int nkt,
+    int Sq, int Sk, int causal, int64_t mult, unsigned long long* counts, int* status) {
+  __shared__ unsigned long long red[3][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t lrow = blockIdx.x;          // list row: head * nqt + query tile
+  const int qt = static_cast<int>(lrow % nqt);
+  const int64_t shift = int64_t(Sk) - Sq;   // bottom-right causal alignment
+  int beg = 0, end = nkt;
+  if (row_ptr != nullptr) {
+    beg = row_ptr[lrow];
+    end = row_ptr[lrow + 1];
+  }
+  unsigned long long listed = 0, partial = 0, pairs = 0;
+  for (int n = beg + warp; n < end; n += 8) {
+    const int kt = row_ptr != nullptr ? col_idx[n] : n;
+    if (kt < 0 || kt >= nkt) {
+      if (lane == 0) record_status(status, dev_code(kDevBadList, kKerBlockmask, 3));
+      continue;
+    }
+    const int pb = tile_bits != nullptr ? tile_bits[n] : -1;
+    const int64_t k0 = int64_t(kt) * kTile;
+    unsigned long long cnt = 0;
+    if (pb < 0) {
+      const int64_t k1 = min64(Sk, k0 + kTile);
+      for (int rr = lane; rr < kTile; rr += 32) {
+        const int64_t r = int64_t(qt) * kTile + rr;
+        if (r >= Sq) break;
+        const int64_t lim = causal ? min64(k1, r + 1 + shift) : k1;
+        if (lim > k0) cnt += static_cast<unsigned long long>(lim - k0);
+      }
+    } else {
+      const uint64_t* w = bits + int64_t(pb) * 256;
+      for (int wi = lane; wi < 256; wi += 32) {
+        uint64_t word = w[wi];
+        if (causal) {
+          // bit 8 r + c is row qt*128 + 8 rb + r, key k0 + 8 cb + c
+          const int rb = wi >> 4, cb = wi & 15;
+          uint64_t keep = 0;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int64_t last = int64_t(qt) * kTile + 8 * rb + r + shift - (k0 + 8 * cb);
+            const uint64_t byte = last < 0 ? 0u : last >= 7 ? 0xffu : ((1u << (last + 1)) - 1u);
+            keep |= byte << (8 * r);
+          }
+          word &= keep;
+        }
+        cnt += static_cast<unsigned long long>(__popcll(word));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (cnt > 0) {
+      listed += 1;
+      partial += pb >= 0 ? 1 : 0;
+      pairs += cnt;
+    }
+  }
+  if (lane == 0) {
+    red[0][warp] = listed;
+    red[1][warp] = partial;
+    red[2][warp] = pairs;
+  }
+  __syncthreads();
+  if (threadIdx.x < 3) {
+    unsigned long long t = 0;
+    for (int w = 0; w < 8; ++w) t += red[threadIdx.x][w];
+    if (t != 0) atomicAdd(counts + threadIdx.x, t * static_cast<unsigned long long>(mult));
+  }
+}
+
+cudaError_t launch_blockmask_counts(const int32_t* row_ptr, const int32_t* col_idx,
+                                    const int32_t* tile_bits, const uint64_t* bits, int per_head,
+                                    int B, int H, int Sq, int Sk, int causal, int64_t* counts,
+                                    cudaStream_t s, int* status) {
+  cudaError_t e = cudaMemsetAsync(counts, 0, 3 * sizeof(int64_t), s);
+  if (e != cudaSuccess || Sq == 0 || Sk == 0) return e;
+  const int nqt = (Sq + kTile - 1) / kTile, nkt = (Sk + kTile - 1) / kTile;
+  const bool each_head = row_ptr != nullptr && per_head;
+  const int64_t rows = (each_head ? int64_t(B) * H : 1) * nqt;
+  const int64_t mult = each_head ? 1 : int64_t(B) * H;
+  if (rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  blockmask_counts_kernel<<<static_cast<unsigned>(rows), 256, 0, s>>>(
+      row_ptr, col_idx, tile_bits, bits, nqt, nkt, Sq, Sk, causal, mult,
+      reinterpret_cast<unsigned long long*>(counts), status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, int Sk,
                                             int32_t* row_ptr, int32_t* col_idx,
                                             int32_t* tile_bits, uint64_t* bits, int64_t bits_cap,

@@ -348,10 +348,17 @@ __global__ void __launch_bounds__(kThreads) decode_partials_kernel(
 // Lane s computes split s's weight exp(lse_s - LSE) once (32 splits at a time)
 // and the weights are broadcast by shuffles; each lane then accumulates its
 // columns with 16-byte loads when the row allows it.
-__device__ __forceinline__ float merge_max(const float* lp, int nsplit) {
+// Partial s of row r sits at o_part[s * o_split + r * o_row] (d floats) and
+// lse_part[s * l_split + r * l_row]: row-major [rows, nsplit] as the decode
+// workspace stores it, or split-major [nsplit, rows] as gathered from ranks.
+struct MergeStrides {
+  int64_t o_split, o_row, l_split, l_row;
+};
+
+__device__ __forceinline__ float merge_max(const float* lp, int nsplit, int64_t l_split) {
   const int lane = threadIdx.x & 31;
   float M = kNegInf;
-  for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, lp[s]);
+  for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, lp[s * l_split]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   return M;
@@ -362,20 +369,21 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
                                                            const float* __restrict__ lse_part,
                                                            TO* __restrict__ o,
                                                            float* __restrict__ lse, int64_t rows,
-                                                           int nsplit, int d) {
+                                                           int nsplit, int d,
+                                                           const MergeStrides st) {
   const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const float* lp = lse_part + row * nsplit;
-  const float M = merge_max(lp, nsplit);
+  const float* lp = lse_part + row * st.l_row;
+  const float M = merge_max(lp, nsplit, st.l_split);
   // sum of exp(lse_s - M)
   float tot = 0.f;
   if (M != kNegInf)
-    for (int s = lane; s < nsplit; s += 32) tot += expf(lp[s] - M);
+    for (int s = lane; s < nsplit; s += 32) tot += expf(lp[s * st.l_split] - M);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const float LSE = (M != kNegInf) ? M + logf(tot) : kNegInf;
-  const float* op = o_part + row * int64_t(nsplit) * d;
+  const float* op = o_part + row * st.o_row;
   if constexpr (kVec4) {
     // lane owns columns [4c, 4c + 4) for c = lane, lane + 32, ...
     for (int c0 = 0; c0 < d; c0 += 128) {
@@ -383,13 +391,13 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int s0 = 0; s0 < nsplit; s0 += 32) {
         const int s = s0 + lane;
-        const float ls = s < nsplit ? lp[s] : kNegInf;
+        const float ls = s < nsplit ? lp[s * st.l_split] : kNegInf;
         const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
         const int n = min(32, nsplit - s0);
         for (int k = 0; k < n; ++k) {
           const float wk = __shfl_sync(0xffffffffu, w, k);
           if (c < d && wk != 0.f) {
-            const float4 v = *reinterpret_cast<const float4*>(op + int64_t(s0 + k) * d + c);
+            const float4 v = *reinterpret_cast<const float4*>(op + int64_t(s0 + k) * st.o_split + c);
             acc.x = fmaf(wk, v.x, acc.x);
             acc.y = fmaf(wk, v.y, acc.y);
             acc.z = fmaf(wk, v.z, acc.z);
@@ -410,12 +418,12 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
       float acc = 0.f;
       for (int s0 = 0; s0 < nsplit; s0 += 32) {
         const int s = s0 + lane;
-        const float ls = s < nsplit ? lp[s] : kNegInf;
+        const float ls = s < nsplit ? lp[s * st.l_split] : kNegInf;
         const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
         const int n = min(32, nsplit - s0);
         for (int k = 0; k < n; ++k) {
           const float wk = __shfl_sync(0xffffffffu, w, k);
-          if (c < d && wk != 0.f) acc = fmaf(wk, op[int64_t(s0 + k) * d + c], acc);
+          if (c < d && wk != 0.f) acc = fmaf(wk, op[int64_t(s0 + k) * st.o_split + c], acc);
         }
       }
       if (c < d) o[row * d + c] = static_cast<TO>(acc);
@@ -461,27 +469,37 @@ cudaError_t launch_decode_partials(const void* q, const void* k, const void* v, 
   return launch_d<64>(q, k, v, o_part, lse_part, B, H, Hkv, Sk, scale, nsplit, s, status);
 }
 
-cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void* o, float* lse,
-                                int64_t rows, int nsplit, int d, rf_dtype out_dt, cudaStream_t s) {
+cudaError_t launch_splitk_merge_strided(const float* o_part, const float* lse_part, void* o,
+                                        float* lse, int64_t rows, int nsplit, int d,
+                                        int64_t o_split, int64_t o_row, int64_t l_split,
+                                        int64_t l_row, rf_dtype out_dt, cudaStream_t s) {
   const int warps = 4;
   const int64_t grid = (rows + warps - 1) / warps;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const bool vec = d % 4 == 0 && reinterpret_cast<uintptr_t>(o_part) % 16 == 0;
+  const MergeStrides st{o_split, o_row, l_split, l_row};
+  const bool vec = d % 4 == 0 && reinterpret_cast<uintptr_t>(o_part) % 16 == 0 &&
+                   o_split % 4 == 0 && o_row % 4 == 0;
   const unsigned g = static_cast<unsigned>(grid);
   if (out_dt == RF_F32) {
     float* of = static_cast<float*>(o);
     if (vec)
-      splitk_merge_kernel<float, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d);
+      splitk_merge_kernel<float, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d, st);
     else
-      splitk_merge_kernel<float, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d);
+      splitk_merge_kernel<float, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d, st);
   } else {
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
     if (vec)
-      splitk_merge_kernel<__nv_bfloat16, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d);
+      splitk_merge_kernel<__nv_bfloat16, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d, st);
     else
-      splitk_merge_kernel<__nv_bfloat16, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d);
+      splitk_merge_kernel<__nv_bfloat16, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d, st);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                                int64_t rows, int nsplit, int d, rf_dtype out_dt, cudaStream_t s) {
+  return launch_splitk_merge_strided(o_part, lse_part, o, lse, rows, nsplit, d, d,
+                                     int64_t(nsplit) * d, 1, nsplit, out_dt, s);
 }
 
 }  // namespace rf

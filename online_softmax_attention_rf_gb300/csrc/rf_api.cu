@@ -349,6 +349,29 @@ rf_status rf_attn_decode_splitk(const void* q, const void* k, const void* v, voi
   return ok();
 }
 
+rf_status rf_attn_decode_partials(const void* q, const void* k, const void* v, float* ws,
+                                  size_t ws_bytes, int B, int H, int Hkv, int Sk, int d,
+                                  float scale, int nsplit, rf_dtype dt, rf_stream stream) {
+  const char* fn = "rf_attn_decode_partials";
+  // o is not written: q stands in for it in the shared checks
+  const rf_status chk =
+      rf::check_decode_args(fn, q, k, v, q, nullptr, B, H, Hkv, Sk, d, scale, nsplit, dt);
+  if (chk != RF_OK) return chk;
+  if (ws == nullptr) return fail(RF_ERR_INVALID, "%s: NULL pointer", fn);
+  if (!aligned(ws, 16)) return fail(RF_ERR_INVALID, "%s: ws must be 16-byte aligned", fn);
+  if (ws_bytes < rf_decode_workspace_bytes(B, H, nsplit, d))
+    return fail(RF_ERR_INVALID, "%s: workspace too small (%zu < %zu)", fn, ws_bytes,
+                rf_decode_workspace_bytes(B, H, nsplit, d));
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "%s: no CUDA device", fn);
+  float* o_part = ws;
+  float* lse_part = ws + size_t(B) * H * nsplit * d;
+  cudaError_t e = rf::launch_decode_partials(q, k, v, o_part, lse_part, B, H, Hkv, Sk, d, scale,
+                                             nsplit, reinterpret_cast<cudaStream_t>(stream), st);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_attn_decode_partials: launch");
+  return ok();
+}
+
 rf_status rf_splitk_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                           int64_t rows, int nsplit, int d, rf_dtype out_dt, rf_stream stream) {
   if (rows < 0 || nsplit < 1 || d < 1 || d > 1024)
@@ -368,6 +391,30 @@ rf_status rf_splitk_merge(const float* o_part, const float* lse_part, void* o, f
   return ok();
 }
 
+rf_status rf_splitk_merge_strided(const float* o_part, const float* lse_part, void* o, float* lse,
+                                  int64_t rows, int nsplit, int d, int64_t o_split_stride,
+                                  int64_t o_row_stride, int64_t lse_split_stride,
+                                  int64_t lse_row_stride, rf_dtype out_dt, rf_stream stream) {
+  const char* fn = "rf_splitk_merge_strided";
+  if (rows < 0 || nsplit < 1 || d < 1 || d > 1024)
+    return fail(RF_ERR_INVALID, "%s: bad sizes", fn);
+  if (out_dt != RF_F32 && out_dt != RF_BF16) return fail(RF_ERR_INVALID, "%s: bad dtype", fn);
+  if (o_split_stride < 0 || o_row_stride < 0 || lse_split_stride < 0 || lse_row_stride < 0)
+    return fail(RF_ERR_INVALID, "%s: strides must be >= 0", fn);
+  if (rows == 0) return ok();
+  if (rows > INT32_MAX) return fail(RF_ERR_INVALID, "%s: rows > 2^31-1", fn);
+  if (o_part == nullptr || lse_part == nullptr || o == nullptr)
+    return fail(RF_ERR_INVALID, "%s: NULL pointer", fn);
+  if (!aligned(o_part, 4) || !aligned(lse_part, 4) || !aligned(o, out_dt == RF_F32 ? 4 : 2) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return fail(RF_ERR_INVALID, "%s: misaligned pointer", fn);
+  cudaError_t e = rf::launch_splitk_merge_strided(
+      o_part, lse_part, o, lse, rows, nsplit, d, o_split_stride, o_row_stride, lse_split_stride,
+      lse_row_stride, out_dt, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_splitk_merge_strided: launch");
+  return ok();
+}
+
 rf_status rf_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt, int32_t* row_ptr,
                              int32_t* col_idx, int64_t col_cap, rf_stream stream) {
   if (nheads < 1 || nqt < 1 || nkt < 1 || col_cap < 0)
@@ -383,6 +430,40 @@ rf_status rf_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
   cudaError_t e = rf::launch_blockmask_build(dense, nheads, nqt, nkt, row_ptr, col_idx, col_cap,
                                              reinterpret_cast<cudaStream_t>(stream), st);
   if (e != cudaSuccess) return cuda_fail(e, "rf_blockmask_build: launch");
+  return ok();
+}
+
+rf_status rf_blockmask_counts(const rf_blockmask* bm, int B, int H, int Sq, int Sk, int causal,
+                              int64_t* counts, rf_stream stream) {
+  const char* fn = "rf_blockmask_counts";
+  if (B < 1 || H < 1 || Sq < 0 || Sk < 0 || Sq > (1 << 30) || Sk > (1 << 30))
+    return fail(RF_ERR_INVALID, "%s: bad sizes B=%d H=%d Sq=%d Sk=%d", fn, B, H, Sq, Sk);
+  if (causal != 0 && causal != 1) return fail(RF_ERR_INVALID, "%s: causal must be 0/1", fn);
+  if (counts == nullptr || !aligned(counts, 8))
+    return fail(RF_ERR_INVALID, "%s: counts must be an 8-byte aligned device int64[3]", fn);
+  const int nqt = static_cast<int>(cdiv(Sq, 128)), nkt = static_cast<int>(cdiv(Sk, 128));
+  if (bm != nullptr) {
+    if (bm->tile_q != 128 || bm->tile_k != 128)
+      return fail(RF_ERR_INVALID, "%s: blockmask tiles must be 128x128", fn);
+    if (bm->nqt != nqt || bm->nkt != nkt)
+      return fail(RF_ERR_INVALID, "%s: blockmask nqt/nkt (%d,%d) != (%d,%d)", fn, bm->nqt,
+                  bm->nkt, nqt, nkt);
+    if (bm->per_head != 0 && bm->per_head != 1)
+      return fail(RF_ERR_INVALID, "%s: blockmask per_head must be 0/1", fn);
+    if (Sq > 0 && Sk > 0 && (bm->row_ptr == nullptr || bm->col_idx == nullptr))
+      return fail(RF_ERR_INVALID, "%s: blockmask lists are NULL", fn);
+    if (bm->tile_bits != nullptr && bm->bits == nullptr)
+      return fail(RF_ERR_INVALID, "%s: blockmask tile_bits without bits", fn);
+    if (bm->bits != nullptr && !aligned(bm->bits, 8))
+      return fail(RF_ERR_INVALID, "%s: blockmask bits must be 8-byte aligned", fn);
+  }
+  int* st = rf::status_word();
+  if (st == nullptr) return fail(RF_ERR_CUDA, "%s: no CUDA device", fn);
+  cudaError_t e = rf::launch_blockmask_counts(
+      bm ? bm->row_ptr : nullptr, bm ? bm->col_idx : nullptr, bm ? bm->tile_bits : nullptr,
+      bm ? bm->bits : nullptr, bm ? bm->per_head : 0, B, H, Sq, Sk, causal, counts,
+      reinterpret_cast<cudaStream_t>(stream), st);
+  if (e != cudaSuccess) return cuda_fail(e, "rf_blockmask_counts: launch");
   return ok();
 }
 

@@ -105,6 +105,12 @@ cudaError_t launch_decode_partials(const void* q, const void* k, const void* v, 
 cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                                 int64_t rows, int nsplit, int d, rf_dtype out_dt,
                                 cudaStream_t s);
+// Partial s of row r at o_part + s * o_split + r * o_row and
+// lse_part[s * l_split + r * l_row] (element strides).
+cudaError_t launch_splitk_merge_strided(const float* o_part, const float* lse_part, void* o,
+                                        float* lse, int64_t rows, int nsplit, int d,
+                                        int64_t o_split, int64_t o_row, int64_t l_split,
+                                        int64_t l_row, rf_dtype out_dt, cudaStream_t s);
 cudaError_t launch_blockmask_build(const uint8_t* dense, int nheads, int nqt, int nkt,
                                    int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
                                    cudaStream_t s, int* status);
@@ -123,6 +129,10 @@ cudaError_t launch_moment_of_inertia(const float* points, const float* masses, i
                                      cudaStream_t s);
 cudaError_t launch_row_moments(const void* x, int64_t rows, int64_t cols, float eps, float* mean,
                                float* var, void* y, rf_dtype dt, cudaStream_t s);
+cudaError_t launch_blockmask_counts(const int32_t* row_ptr, const int32_t* col_idx,
+                                    const int32_t* tile_bits, const uint64_t* bits, int per_head,
+                                    int B, int H, int Sq, int Sk, int causal, int64_t* counts,
+                                    cudaStream_t s, int* status);
 cudaError_t launch_blockmask_build_elements(const uint8_t* dense, int nheads, int Sq, int Sk,
                                             int32_t* row_ptr, int32_t* col_idx,
                                             int32_t* tile_bits, uint64_t* bits, int64_t bits_cap,

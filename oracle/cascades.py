@@ -13,7 +13,9 @@ Sources (page title, section):
   the Korean page, results: variance and moment-of-inertia (non-ML)
   workloads.
 
-Readings where the pages are silent (each listed in the design notes):
+Readings where the pages are silent (the pages name these workloads but
+give no formula, format or precision; each reading below is the plainest
+one for a workload given by name):
 
 * MoE routing: p = softmax(logits) over the experts of one token; the k
   experts with the largest p are selected, in descending order, ties broken
@@ -36,9 +38,15 @@ Readings where the pages are silent (each listed in the design notes):
   (reduction 1); the row is scaled by 448 / amax and rounded to the nearest
   E4M3 value, ties to even, magnitudes past 448 saturating to 448; the row's
   dequantisation scale is amax / 448 (an all-zero row: codes 0, scale 1).
-  Because the rounding decides an integer code, it is taken in float32, as
-  the kernel computes it: inv = float32(448) / float32(amax), then
-  float32(x) * inv. The GEMM (reduction 2, over the quantised values) is
+  The pages fix no precision for the scaled value. Because the rounding
+  decides an integer code, the oracle takes that one decision in float32,
+  the precision in which the kernel forms it: inv = float32(448) /
+  float32(amax), then float32(x) * inv. Everything else (amax, the E4M3
+  rounding of that product, the GEMM) is exact or float64. Taken in float64
+  instead, the scaled value differs from the float32 one by at most about
+  two float32 ulps, so the codes agree except where the product lies within
+  that distance of a rounding tie between two E4M3 values (a pin checks
+  exactly this). The GEMM (reduction 2, over the quantised values) is
   C[m, n] = sa[m] * sw[n] * sum_k qa[m, k] qw[n, k], in float64 here.
 """
 

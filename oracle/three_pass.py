@@ -27,7 +27,9 @@ The oracle deliberately does NOT use the incremental (online) form the GPU
 uses; it runs the definition: pass 1 row maximum, pass 2 sum of shifted
 exponentials, pass 3 normalised P.V.
 
-Readings where the pages are silent (each listed in the design notes):
+Readings where the pages are silent (none of these pages prints a formula,
+a bit order or a layout; each reading below is the plainest one that the
+rest of the pages' text supports):
 
 * LSE is the natural log: LSE_i = m_i + ln l_i.
 * Causal masking is bottom-right aligned: query row i sees key j iff

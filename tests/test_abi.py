@@ -304,3 +304,52 @@ def test_no_cpu_fallback(L, monkeypatch):
         api.lib()
     with pytest.raises(RuntimeError):
         api.decode_workspace_bytes(1, 1, 1, 64)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ws=None), api.RF_ERR_INVALID),
+    (dict(ws=MIS), api.RF_ERR_INVALID),
+    (dict(ws_bytes=16), api.RF_ERR_INVALID),
+    (dict(q=None), api.RF_ERR_INVALID),
+    (dict(Hkv=3), api.RF_ERR_INVALID),
+    (dict(nsplit=1001), api.RF_ERR_INVALID),
+    (dict(dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
+])
+def test_decode_partials_rejects(L, kw, expect):
+    a = dict(q=A, k=A, v=A, ws=A, ws_bytes=None, B=2, H=8, Hkv=2, Sk=1000, d=128, scale=0.1,
+             nsplit=4, dt=api.RF_BF16)
+    a.update(kw)
+    if a["ws_bytes"] is None:
+        a["ws_bytes"] = api.decode_workspace_bytes(a["B"], a["H"], a["nsplit"], a["d"])
+    assert L.rf_attn_decode_partials(a["q"], a["k"], a["v"], a["ws"], a["ws_bytes"], a["B"],
+                                     a["H"], a["Hkv"], a["Sk"], a["d"], a["scale"], a["nsplit"],
+                                     a["dt"], None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A, A, A, A, 5, 0, 64, 64, 0, 1, 5), api.RF_ERR_INVALID),        # nsplit 0
+    ((A, A, A, A, 5, 4, 64, -64, 256, 1, 4), api.RF_ERR_INVALID),     # negative stride
+    ((A, A, A, A, 5, 4, 64, 64, 256, 1, -1), api.RF_ERR_INVALID),
+    ((None, A, A, A, 5, 4, 64, 64, 256, 1, 4), api.RF_ERR_INVALID),
+    ((A, A, A, A + 2, 5, 4, 64, 64, 256, 1, 4), api.RF_ERR_INVALID),  # misaligned lse
+    ((A, A, A, A, 0, 4, 64, 64, 256, 1, 4), api.RF_OK),               # no rows: no launch
+])
+def test_merge_strided_validation(L, args, expect):
+    o_part, lse_part, o, lse, rows, nsplit, d, os_, or_, ls_, lr_ = args
+    assert L.rf_splitk_merge_strided(o_part, lse_part, o, lse, rows, nsplit, d, os_, or_, ls_,
+                                     lr_, api.RF_F32, None) == expect
+
+
+def test_blockmask_counts_validation(L):
+    f = L.rf_blockmask_counts
+    assert f(None, 0, 1, 128, 128, 0, A, None) == api.RF_ERR_INVALID          # B
+    assert f(None, 1, 1, -1, 128, 0, A, None) == api.RF_ERR_INVALID          # Sq
+    assert f(None, 1, 1, 128, 128, 2, A, None) == api.RF_ERR_INVALID          # causal
+    assert f(None, 1, 1, 128, 128, 0, None, None) == api.RF_ERR_INVALID       # counts
+    assert f(None, 1, 1, 128, 128, 0, A + 4, None) == api.RF_ERR_INVALID      # alignment
+    bm = api.RFBlockMask(128, 128, 2, 2, A, A, 0)
+    assert f(ctypes.byref(bm), 1, 1, 128, 128, 0, A, None) == api.RF_ERR_INVALID  # nqt != 1
+    bm = api.RFBlockMask(128, 128, 1, 1, None, A, 0)
+    assert f(ctypes.byref(bm), 1, 1, 128, 128, 0, A, None) == api.RF_ERR_INVALID  # NULL lists
+    bm = api.RFBlockMask(64, 128, 1, 1, A, A, 0)
+    assert f(ctypes.byref(bm), 1, 1, 128, 128, 0, A, None) == api.RF_ERR_INVALID  # tile side

@@ -3,7 +3,10 @@
 STOF, Méthodologie, unified MHA module, kernel selection: the row-wise kernel
 for highly sparse masks on short sequences, the block-wise kernel otherwise.
 rf_attn_choose_kernel / rf_attn_estimate_us are pure host functions of the
-library; selector_counts is the binding's count of their inputs.
+library. Their inputs (listed tiles, partial tiles, visible pairs) come from
+rf_blockmask_counts on the device; here they are counted by enumeration, and
+tests/test_gpu_selector.py checks the device counts against the same
+enumeration.
 """
 
 import numpy as np
@@ -18,7 +21,7 @@ def _lib():
     api.lib()
 
 
-def _brute_counts(B, H, Sq, Sk, causal, em):
+def brute_counts(B, H, Sq, Sk, causal, em):
     """Counts by enumerating tiles (em [nh, Sq, Sk] after any causal limit)."""
     listed = partial = 0
     for hm in em:
@@ -61,8 +64,7 @@ def test_scattered_short_workload_picks_the_block_kernel():
     on GB300 (0.19 ms against 0.93 ms for the row-wise kernel)."""
     w = inputs.WORKLOADS["scattered_short"]
     em = inputs.scattered_mask(w["Sq"], w["window"], w["n_global"], w["density"], w["seed"])
-    bm = api.BlockMask(None, None, 8, 8, 0, host_mask=("elements", em[None]))
-    counts = api.selector_counts(w["B"], w["H"], w["Sq"], w["Sk"], False, bm)
+    counts = brute_counts(w["B"], w["H"], w["Sq"], w["Sk"], False, em[None])
     assert api.choose_kernel(w["B"], w["H"], w["Sq"], w["Sk"], w["d"], *counts, num_sms=152) == \
         api.RF_KERNEL_BLOCKWISE
 
@@ -71,8 +73,7 @@ def test_tiny_scattered_masks_pick_the_row_kernel():
     """A highly sparse mask on a short sequence with one head: the block-wise
     kernel would run one CTA on one of 152 SMs; the model picks row-wise."""
     em = inputs.scattered_mask(256, 4, 2, 0.002, 3)
-    bm = api.BlockMask(None, None, 2, 2, 0, host_mask=("elements", em[None]))
-    counts = api.selector_counts(1, 1, 256, 256, False, bm)
+    counts = brute_counts(1, 1, 256, 256, False, em[None])
     assert api.choose_kernel(1, 1, 256, 256, 64, *counts, num_sms=152) == api.RF_KERNEL_ROWWISE
 
 
@@ -85,27 +86,3 @@ def test_estimates_are_monotone():
     assert b2 > b1 and r2 > r1          # partial tiles and more pairs
     b3, r3 = api.estimate_us(*base.values(), 2000, 0, 10 ** 7, 76)
     assert b3 >= b1 and r3 > r1         # fewer SMs
-
-
-@pytest.mark.parametrize("causal", [False, True])
-def test_selector_counts_match_enumeration(causal):
-    Sq, Sk = 300, 420
-    rng = np.random.default_rng(3)
-    em = rng.random((2, Sq, Sk)) < 0.01
-    em[:, :128, :128] = True                            # one full tile per head
-    vis = np.arange(Sk)[None, :] <= np.arange(Sq)[:, None] + (Sk - Sq) if causal else \
-        np.ones((Sq, Sk), dtype=bool)
-    bm = api.BlockMask(None, None, 3, 4, 1, host_mask=("elements", em))
-    got = api.selector_counts(1, 2, Sq, Sk, causal, bm)
-    listed, _, visible = _brute_counts(1, 2, Sq, Sk, causal, em & vis)
-    _, partial, _ = _brute_counts(1, 2, Sq, Sk, False, em)
-    assert got[0] == listed and got[2] == visible
-    # partial counts tiles that are partial in the encoding and still listed
-    assert got[1] <= partial and got[1] <= got[0]
-    tm = rng.random((3, 4)) < 0.5
-    bmt = api.BlockMask(None, None, 3, 4, 0, host_mask=("tiles", tm[None]))
-    full = np.repeat(np.repeat(tm, 128, 0), 128, 1)[:Sq, :Sk][None] & vis
-    assert api.selector_counts(2, 3, Sq, Sk, causal, bmt) == \
-        (_brute_counts(2, 3, Sq, Sk, causal, full)[0], 0, int(full.sum()) * 6)
-    dense = api.selector_counts(2, 3, Sq, Sk, causal, None)
-    assert dense[2] == int(vis.sum()) * 6 and dense[1] == 0
