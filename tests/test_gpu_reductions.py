@@ -90,9 +90,12 @@ def test_merge_matches_oracle(cuda_device, rows, nsplit, d):
     assert_close(ob, o_ref, 8e-3 * max(1.0, float(np.abs(o_ref).max())), "O bf16")
 
 
+# (300, 32768) and (200, 40000) (bf16: 3 pieces, the last one partial) give
+# every cluster of the persistent on-chip path several rows, so its ring of
+# pieces wraps at many offsets
 SOFTMAX_SHAPES = [
     (7, 33), (64, 1000), (3, 1), (16, 16384), (2, 32768), (3, 40000), (2, 262144),
-    (1, 300001), (2, 600000), (5, 4099)]
+    (1, 300001), (2, 600000), (5, 4099), (300, 32768), (200, 40000)]
 
 
 @pytest.mark.parametrize("rows,cols", SOFTMAX_SHAPES)
