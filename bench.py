@@ -66,10 +66,11 @@ TRAFFIC = {
     "attn_tc_scattered_short": {"digest": "8dc32d453b50a32d", "bytes": 112646656,
                                 "sources": ("attn_tc.cu", "rf_device.cuh")},
     # softmax_rows kernels: dram__bytes_read.sum + dram__bytes_write.sum
-    # (rows_64k: 1073.9 + 1014.1 MB; rows_1m, clusters of 8: 1401.8 + 1015.8 MB)
+    # (rows_64k: 1073.9 + 1014.1 MB; rows_1m, clusters of 8, second pass back
+    # to front: 1366.6 + 1013.9 MB)
     "softmax_rows_64k": {"digest": "500902232009bba1", "bytes": 2088053504,
                          "sources": ("softmax_rows.cu", "rf_device.cuh")},
-    "softmax_rows_1m": {"digest": "500902232009bba1", "bytes": 2417586176,
+    "softmax_rows_1m": {"digest": "b278a7aa1a83890f", "bytes": 2380536064,
                         "sources": ("softmax_rows.cu", "rf_device.cuh")},
     # moe_route_sorted_kernel<float, 8>, row_moments_smem_kernel<float> and
     # inertia_kernel: dram__bytes_read.sum + dram__bytes_write.sum

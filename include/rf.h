@@ -108,12 +108,10 @@ typedef struct {
  * (maximum, then sum of exponentials). A row that fits one CTA (up to
  * 64 KB: cols <= 16384 for f32) is held in shared memory between the
  * reductions and the write: one read and one write of x per element in HBM.
- * A longer row is split over a cluster of 2..8 CTAs, which exchange
- * (max, sum) pairs through distributed shared memory (multi-segment
- * strategy). When x and y are 16-byte aligned and the row splits into equal
- * slices of whole 16-byte vectors of at most 128 KB (rows up to 1 MiB), each
- * slice stays in shared memory until y is written: again 1 read + 1 write.
- * Other long rows read their slice a second time, mostly from L2.
+ * A longer row is split over a cluster of 2..8 CTAs (64 KB or more each).
+ * They exchange (max, sum) pairs through distributed shared memory
+ * (multi-segment strategy), then read their slice a second time, mostly from
+ * L2 where the first read left it.
  *  x, y : [rows, cols] row-major, dtype dt (RF_F32 or RF_BF16); may alias.
  *  rows >= 0, cols >= 0 (either 0: nothing is launched, RF_OK).
  * A row whose entries are all -inf yields zeros. Errors: RF_ERR_INVALID for

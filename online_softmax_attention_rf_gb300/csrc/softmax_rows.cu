@@ -13,17 +13,20 @@
 //    mbarrier so the maximum starts on the first piece), then
 //    m = max, p = exp(x - m) written back in place with l = sum p, and
 //    y = p / l stored -- 1 read + 1 write of HBM per element;
-//  * longer rows, one cluster of 2..8 CTAs per row (multi-segment): each
-//    thread folds its elements into a running (m, l) (the incremental form,
-//    O(1) state), the CTAs exchange their (m_c, l_c) through distributed
-//    shared memory and combine them as L = sum_c l_c exp(m_c - M), then y is
-//    written. When the row splits into 16-byte-aligned slices of at most
-//    128 KB, the slice stays on chip (softmax_rows_ring: persistent clusters
-//    over the rows, a ring of 16 KB pieces filled by a producer warp, the
-//    next row's loads overlapping this row's exchange and stores): 1 read +
-//    1 write of HBM per element. Otherwise (unaligned rows, slices over
-//    128 KB) a second pass re-reads the slice, the first pass loading with an
-//    L2 evict-last policy so that the second mostly finds it in L2.
+//  * longer rows, one cluster of 2..8 CTAs per row (multi-segment), about
+//    128 KB of the row per CTA: each thread folds its elements into a running
+//    (m, l) (the incremental form, O(1) state), the CTAs exchange their
+//    (m_c, l_c) through distributed shared memory and combine them as
+//    L = sum_c l_c exp(m_c - M), and a second pass over the slice, back to
+//    front, writes y. The first pass loads with an L2 evict-last policy and
+//    the second with evict-first, so most of the slice is re-read from the
+//    126 MB L2 rather than HBM (about 1.13 x the 1 read + 1 write per
+//    element in DRAM on 1 MiB rows). Keeping the slice in shared memory
+//    instead measured slower on this GPU: a 128 KB slice leaves one CTA per
+//    SM, only 120 SMs can hold clusters of 8 such CTAs, and with the slice
+//    resident too little of the next row can be in flight (a persistent
+//    cluster ring with a producer warp reached 4.3 TB/s on 1 MiB rows,
+//    against 5.6 TB/s here).
 // x and y may alias: every element is read before the thread that writes it
 // writes it.
 #include <cooperative_groups.h>
@@ -328,7 +331,10 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y
     const uint4* xv = reinterpret_cast<const uint4*>(xr + seg0);
     uint4* yv = reinterpret_cast<uint4*>(yr + seg0);
     const int64_t nv = (seg1 - seg0) / V;
-    for (int64_t b = threadIdx.x; b < nv; b += U * kThreads) {
+    // back to front: the last vectors pass 1 loaded are the likeliest still in L2
+    const int64_t nblk = (nv + U * kThreads - 1) / (U * kThreads);
+    for (int64_t bb = nblk - 1; bb >= 0; --bb) {
+      const int64_t b = bb * U * kThreads + threadIdx.x;
       uint4 w[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
@@ -360,253 +366,6 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_stream(const T* x, T* y
   }
 }
 
-// ---------------------------------------------------------------------------
-// Long rows with the slice kept on chip: persistent clusters and a ring.
-//
-// One cluster of nc CTAs per row (multi-segment strategy), each CTA holding
-// its slice of cols / nc elements (at most kRingSliceBytes) in shared memory
-// from the moment it lands until y is written: 1 read + 1 write of HBM per
-// element. A grid of co-resident clusters walks the rows (cluster c takes
-// rows c, c + nclusters, ...), and the slice streams through a ring of
-// kRingSlots pieces of kPiece bytes, filled by one producer warp with bulk
-// copies: as soon as the normalisation of row r has read a piece, its slot
-// takes the next row's data, so the loads of row r + 1 overlap the stores of
-// row r and the cluster exchange, and HBM never waits on one CTA's phases.
-//
-// Per row, the 16 consumer warps
-//  (A) fold each piece into a per-thread running (m, l) as it lands (the
-//      incremental form, O(1) state), then combine the threads (named
-//      barrier 1, consumers only);
-//  (B) push the CTA's (m_c, l_c) into every peer's shared memory and meet at
-//      one cluster barrier (all threads of the cluster, the producer warp
-//      included); every CTA then combines L = sum_c l_c exp(m_c - M);
-//  (C) read their own elements of each piece again from shared memory,
-//      write y = exp(x - M) / L from registers, and release the slot.
-// Each thread reads in (C) exactly the elements it read in (A), so the
-// phases need no CTA barrier between them.
-//
-// Ordering of the exchange: CTA a writes peer b's pairs[r & 1] for row r
-// only after a's wait on the barrier of row r - 1, which b passes only after
-// reading its pairs[(r - 2) & 1]; so a slot is never overwritten before it is
-// read. No CTA leaves before the barrier of its last row, after which no peer
-// writes its shared memory. After a timed-out wait a CTA stops its work
-// (abort flag) but keeps meeting every cluster barrier, so its peers finish.
-constexpr int kRingSlots = 13;                        // 13 x 16 KB = 208 KB
-constexpr int kRingSliceBytes = 128 * 1024;           // at most 8 pieces per slice
-constexpr int kRingConsumers = 512;                   // 16 warps
-constexpr int kRingThreads = kRingConsumers + 32;     // + the producer warp
-
-struct RingSmem {
-  unsigned char data[kRingSlots][kPiece];
-  uint64_t full[kRingSlots];
-  uint64_t empty[kRingSlots];
-  float2 pairs[2][kMaxCluster];
-  float red[2][32];
-  int abort_flag;
-};
-
-// Consumer-only (named barrier 1) reductions over the 16 consumer warps.
-__device__ __forceinline__ float consumers_max(float x, float* red) {
-  x = warp_max(x);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-  asm volatile("bar.sync 1, %0;" ::"n"(kRingConsumers) : "memory");
-  return warp_max((threadIdx.x & 31) < kRingConsumers / 32 ? red[threadIdx.x & 31] : kNegInf);
-}
-__device__ __forceinline__ float consumers_sum(float x, float* red) {
-  x = warp_sum(x);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-  asm volatile("bar.sync 1, %0;" ::"n"(kRingConsumers) : "memory");
-  return warp_sum((threadIdx.x & 31) < kRingConsumers / 32 ? red[threadIdx.x & 31] : 0.f);
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kRingThreads, 1) softmax_rows_ring(const T* x, T* y,
-                                                                    int64_t rows, int64_t cols,
-                                                                    int* status) {
-  constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
-  extern __shared__ __align__(128) unsigned char ring_raw[];
-  RingSmem& sm = *reinterpret_cast<RingSmem*>(ring_raw);
-  cg::cluster_group cl = cg::this_cluster();
-  const int nc = static_cast<int>(cl.num_blocks());
-  const int rank = static_cast<int>(cl.block_rank());
-  const int64_t ncl = gridDim.x / nc, cid = blockIdx.x / nc;
-  const int64_t seg = cols / nc;                                  // elements of the slice
-  const uint32_t slice_bytes = static_cast<uint32_t>(seg * sizeof(T));
-  const int npieces = static_cast<int>((slice_bytes + kPiece - 1) / kPiece);
-  const int64_t my_rows = cid < rows ? (rows - 1 - cid) / ncl + 1 : 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kRingSlots; ++i) {
-      mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], kRingConsumers / 32);
-    }
-    sm.abort_flag = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
-  cluster_arrive_relaxed();  // the start-up phase: every peer is running
-
-  if (warp == kRingConsumers / 32) {
-    // ---------------- producer warp: bulk copies into the ring
-    const uint64_t pol = policy_evict_first();
-    int64_t g = 0;  // pieces issued so far
-    for (int64_t it = 0; it < my_rows; ++it) {
-      // Row it's pieces may need slots that row it - 1's step (C) frees;
-      // the consumers reach (C) once this warp has arrived on the barrier
-      // of row it - 1, which it did at the end of the previous iteration.
-      if (lane == 0 && !sm.abort_flag) {
-        const T* src = x + (cid + it * ncl) * cols + rank * seg;
-        for (int pc = 0; pc < npieces; ++pc, ++g) {
-          const int slot = static_cast<int>(g % kRingSlots);
-          const int64_t use = g / kRingSlots;
-          if (use > 0 && !mbar_wait(&sm.empty[slot], static_cast<uint32_t>((use - 1) & 1),
-                                    status, dev_code(kDevTimeout, kKerSoftmax, 5),
-                                    &sm.abort_flag))
-            break;
-          const uint32_t off = static_cast<uint32_t>(pc) * kPiece;
-          const uint32_t bytes = min(static_cast<uint32_t>(kPiece), slice_bytes - off);
-          mbar_arrive_expect_tx(&sm.full[slot], bytes);
-          bulk_load(sm.data[slot], reinterpret_cast<const unsigned char*>(src) + off, bytes,
-                    &sm.full[slot], pol);
-        }
-      }
-      __syncwarp();
-      cluster_wait_acquire();     // the barrier before row it's exchange (start-up or row it - 1)
-      cluster_arrive_relaxed();   // row it's barrier: the producer publishes nothing
-    }
-    cluster_wait_acquire();       // the last barrier
-    // never leave with copies in flight: the last fill of every used slot
-    if (lane == 0)
-      for (int64_t k = (g > kRingSlots ? g - kRingSlots : 0); k < g; ++k)
-        mbar_wait(&sm.full[k % kRingSlots], static_cast<uint32_t>((k / kRingSlots) & 1), status,
-                  dev_code(kDevTimeout, kKerSoftmax, 6), nullptr);
-    return;
-  }
-
-  // ---------------- consumer warps
-  const uint64_t drop = policy_evict_first();
-  int64_t g0 = 0;  // the row's first piece in the ring sequence
-  for (int64_t it = 0; it < my_rows; ++it, g0 += npieces) {
-    const int64_t row = cid + it * ncl;
-    // (A) local (m, l), piece by piece as they land
-    float m = kNegInf, l = 0.f;
-    if (!sm.abort_flag) {
-      for (int pc = 0; pc < npieces; ++pc) {
-        const int64_t g = g0 + pc;
-        const int slot = static_cast<int>(g % kRingSlots);
-        if (!mbar_wait_warp(&sm.full[slot], static_cast<uint32_t>((g / kRingSlots) & 1), status,
-                            dev_code(kDevTimeout, kKerSoftmax, 7), &sm.abort_flag))
-          break;
-        const int nv = static_cast<int>(min(static_cast<uint32_t>(kPiece),
-                                            slice_bytes - static_cast<uint32_t>(pc) * kPiece) /
-                                        16);
-        const uint4* pv = reinterpret_cast<const uint4*>(sm.data[slot]);
-#pragma unroll
-        for (int u = 0; u < kPiece / 16 / kRingConsumers; ++u) {
-          const int e = threadIdx.x + u * kRingConsumers;
-          if (e < nv) {
-            float v[V];
-            unpack16(pv[e], v);
-            fold(v, m, l);
-          }
-        }
-      }
-    }
-    const float bm = consumers_max(m, sm.red[0]);
-    const float lt = consumers_sum(m == kNegInf ? 0.f : l * ex2_approx((m - bm) * kLog2e),
-                                   sm.red[1]);
-    // (B) exchange (m_c, l_c) with the peers. Before the first row: wait
-    // for the start-up phase (every peer is running). Before row it >= 1 the
-    // wait on row it - 1's barrier (below, last row) already showed that
-    // every peer has read pairs[(it - 2) & 1].
-    if (it == 0) cluster_wait_acquire();
-    float2* pairs = sm.pairs[it & 1];
-    if (threadIdx.x < nc) *cl.map_shared_rank(pairs + rank, threadIdx.x) = make_float2(bm, lt);
-    cluster_arrive_release();
-    cluster_wait_acquire();  // this row's pairs have all landed
-    float M = kNegInf;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, pairs[c].x);
-    float L = 0.f;
-    if (M != kNegInf)
-      for (int c = 0; c < nc; ++c)
-        if (pairs[c].x != kNegInf) L += pairs[c].y * ex2_approx((pairs[c].x - M) * kLog2e);
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const float Ms = (M == kNegInf) ? 0.f : M;
-    // (C) y from the slice on chip; release each piece's slot
-    uint4* yv = reinterpret_cast<uint4*>(y + row * cols + rank * seg);
-    for (int pc = 0; pc < npieces; ++pc) {
-      const int64_t g = g0 + pc;
-      const int slot = static_cast<int>(g % kRingSlots);
-      if (!sm.abort_flag) {
-        const int nv = static_cast<int>(min(static_cast<uint32_t>(kPiece),
-                                            slice_bytes - static_cast<uint32_t>(pc) * kPiece) /
-                                        16);
-        const uint4* pv = reinterpret_cast<const uint4*>(sm.data[slot]);
-#pragma unroll
-        for (int u = 0; u < kPiece / 16 / kRingConsumers; ++u) {
-          const int e = threadIdx.x + u * kRingConsumers;
-          if (e < nv) {
-            float v[V];
-            unpack16(pv[e], v);
-            uint4 o;
-            if constexpr (V == 4) {
-              o = make_uint4(__float_as_uint(exp_shift(v[0], Ms) * inv),
-                             __float_as_uint(exp_shift(v[1], Ms) * inv),
-                             __float_as_uint(exp_shift(v[2], Ms) * inv),
-                             __float_as_uint(exp_shift(v[3], Ms) * inv));
-            } else {
-              uint32_t q[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                q[j] = pack_bf16x2(exp_shift(v[2 * j], Ms) * inv,
-                                   exp_shift(v[2 * j + 1], Ms) * inv);
-              o = make_uint4(q[0], q[1], q[2], q[3]);
-            }
-            st_global_policy(yv + int64_t(pc) * (kPiece / 16) + e, o, drop);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);
-    }
-  }
-  if (my_rows == 0) cluster_wait_acquire();  // the start-up phase
-  // after the last row's barrier no peer writes this CTA's memory any more
-}
-
-// Persistent ring launch: as many clusters as can be resident at once (at
-// most one per row). cudaErrorNotSupported: no cluster of this shape fits, the
-// caller streams instead.
-template <typename T>
-cudaError_t launch_ring(const T* x, T* y, int64_t rows, int64_t cols, int nc, cudaStream_t s,
-                        int* status) {
-  const size_t smem = sizeof(RingSmem);
-  cudaError_t e = cudaFuncSetAttribute(softmax_rows_ring<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = nc;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.stream = s;
-  cfg.blockDim = dim3(kRingThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.gridDim = dim3(static_cast<unsigned>(nc));
-  int active = 0;
-  e = cudaOccupancyMaxActiveClusters(&active, softmax_rows_ring<T>, &cfg);
-  if (e != cudaSuccess) return e;
-  if (active < 1) return cudaErrorNotSupported;
-  const int64_t ncl = min64(rows, active);
-  cfg.gridDim = dim3(static_cast<unsigned>(ncl * nc));
-  return cudaLaunchKernelEx(&cfg, softmax_rows_ring<T>, x, y, rows, cols, status);
-}
-
 template <typename T>
 cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStream_t s,
                          int* status, bool fault) {
@@ -624,14 +383,11 @@ cudaError_t launch_typed(const T* x, T* y, int64_t rows, int64_t cols, cudaStrea
         x, y, cols, aligned ? 1 : 0, status, fault ? 1 : 0);
     return cudaGetLastError();
   }
-  // one cluster per row, about one slice per CTA up to kMaxCluster CTAs
-  const int nc = static_cast<int>(min64(kMaxCluster, max64(2, (cols + cap - 1) / cap)));
-  // slices that fit the ring and split the row exactly: keep them on chip
-  if (aligned && cols % (int64_t(nc) * vec) == 0 &&
-      (cols / nc) * int64_t(sizeof(T)) <= kRingSliceBytes) {
-    cudaError_t e = launch_ring<T>(x, y, rows, cols, nc, s, status);
-    if (e != cudaErrorNotSupported) return e;
-  }
+  // one cluster per row, slices of about 128 KB, at most kMaxCluster CTAs
+  // (1 MiB float rows: 8 x 128 KB, which measured 2.6 % faster than
+  // 16 x 64 KB; 512 KB bf16 rows: 4 x 128 KB, 12 % faster than 8 x 64 KB)
+  constexpr int64_t slice = 2 * cap;
+  const int nc = static_cast<int>(min64(kMaxCluster, max64(2, (cols + slice - 1) / slice)));
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -90,9 +90,6 @@ def test_merge_matches_oracle(cuda_device, rows, nsplit, d):
     assert_close(ob, o_ref, 8e-3 * max(1.0, float(np.abs(o_ref).max())), "O bf16")
 
 
-# (300, 32768) and (200, 40000) (bf16: 3 pieces, the last one partial) give
-# every cluster of the persistent on-chip path several rows, so its ring of
-# pieces wraps at many offsets
 SOFTMAX_SHAPES = [
     (7, 33), (64, 1000), (3, 1), (16, 16384), (2, 32768), (3, 40000), (2, 262144),
     (1, 300001), (2, 600000), (5, 4099), (300, 32768), (200, 40000)]
@@ -122,14 +119,15 @@ def test_softmax_rows_edge_values(cuda_device):
     assert_close(xc, y_ref, TOL_F32, "y in place")
 
 
-@pytest.mark.parametrize("cols", [40000, 262144, 600000])
+@pytest.mark.parametrize("cols", [40000, 80000, 262144, 600000])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_softmax_rows_long_rows_masked_in_place(cuda_device, cols, dtype):
-    """Rows longer than 64 KB take the cluster path (2 to 8 CTAs per row, each
-    streaming its slice twice; 40000 columns give clusters of 3 (f32) and 2
-    (bf16), the longer rows clusters of 8): whole slices of -inf, a row with
-    one visible entry and a row with none must combine correctly, in place as
-    well."""
+    """Rows longer than 64 KB take the cluster path (2 to 8 CTAs per row of
+    about 128 KB each, each streaming its slice twice: 80000 float columns
+    give clusters of 3, 40000 columns and the bf16 rows up to 80000 columns
+    clusters of 2, 262144 bf16 columns clusters of 4, the longer rows
+    clusters of 8): whole slices of -inf, a row with one visible entry and a
+    row with none must combine correctly, in place as well."""
     x = inputs.make_rows(3, cols, cols + 11, dtype, 3.0)
     x[0, cols // 3:] = -math.inf          # later CTAs see only -inf
     x[1, :] = -math.inf                   # nothing visible: zeros
