@@ -10,15 +10,16 @@
 // MoE routing (one warp per token): the softmax's maximum and sum of
 // exponentials, then k rounds of arg-max over the logits (top-k of the
 // probabilities are the top-k logits: exp is increasing), ties going to the
-// lower expert index. A round is two single-instruction warp reductions
-// (redux.sync) over order-preserving integer keys of the logits -- the
-// largest key, then the lowest index holding it. With up to eight experts
-// per lane, each lane sorts its slots once (a sorting network) and the winner
-// pops the head of its list. With more, each lane keeps its best and
-// second-best remaining experts; the winner moves to its second best and
-// rescans its slots only when it wins again with the second best not yet
-// known (for random logits, under one rescan per token). The token's logits
-// are read once.
+// lower expert index. Lane l holds the contiguous experts [EPL l, EPL l + EPL)
+// (the logits arrive as 16-byte vectors), so expert order is lane order: in a
+// round, one single-instruction warp reduction (redux.sync) over
+// order-preserving integer keys gives the largest key, and the lowest lane
+// holding it (a ballot and find-first-set) holds the lowest expert index
+// with it. Each lane keeps its best and second-best remaining experts (an
+// ascending scan with strict comparisons keeps the lower slot first); the
+// winner moves to its second best and rescans its slots only when it wins
+// again with the second best not yet known (for random logits, well under
+// one rescan per token). The token's logits are read once.
 //
 // Row moments (one CTA per row): each thread folds its elements into a
 // (count, mean, M2) state, four or eight at a time (two passes over
@@ -95,26 +96,51 @@ __device__ __forceinline__ void route_store(int lane, int64_t t, int k, int reno
   if (lse_out != nullptr && lane == 0) lse_out[t] = m + logf(s);
 }
 
-// 16 or 32 experts per lane: best and second best, rescans when needed.
+// Lane l's EPL logits: 16-byte vector loads when the row allows (vec), else
+// one element at a time; experts past E are -inf.
+template <typename T, int EPL>
+__device__ __forceinline__ void load_block(const T* row, int lane, int E, bool vec,
+                                           float (&x)[EPL]) {
+  const int e0 = lane * EPL;
+  constexpr int V = 16 / sizeof(T);
+  if (vec && e0 + EPL <= E && EPL % V == 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(row + e0);
+#pragma unroll
+    for (int j = 0; j < EPL / V; ++j) {
+      const uint4 w = src[j];
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+      if constexpr (V == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[j * 4 + i] = __uint_as_float(u[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[j * 8 + 2 * i] = __uint_as_float(u[i] << 16);
+          x[j * 8 + 2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) x[i] = e0 + i < E ? load_f(row + e0 + i) : kNegInf;
+  }
+}
+
 template <typename T, int EPL>
 __global__ void __launch_bounds__(256) moe_route_kernel(const T* __restrict__ logits, int64_t T_,
-                                                        int E, int k, int renorm,
+                                                        int E, int k, int renorm, int vec,
                                                         int32_t* __restrict__ idx_out,
                                                         float* __restrict__ w_out,
                                                         float* __restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
   const int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T_) return;  // whole warps leave together
-  const T* row = logits + t * E;
-  // lane l holds experts l, l + 32, ... (coalesced loads); padding gets key 0
+  // real experts get keys >= 1; padding gets 0 and is never selected
   float x[EPL];
+  load_block<T, EPL>(logits + t * E, lane, E, vec != 0, x);
   uint32_t key[EPL];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    x[i] = e < E ? load_f(row + e) : kNegInf;
-    key[i] = e < E ? max(order_key(x[i]), 1u) : 0u;
-  }
+  for (int i = 0; i < EPL; ++i) key[i] = lane * EPL + i < E ? max(order_key(x[i]), 1u) : 0u;
   uint32_t taken = 0u, k1, k2;
   int s1, s2;
   top2<EPL>(key, taken, k1, s1, k2, s2);
@@ -130,18 +156,18 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const T* __restrict__ lo
   for (int i = 0; i < EPL; ++i) s += ex2_approx((x[i] - m) * kLog2e);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  // reduction 3, k rounds: the largest remaining key, then the lowest expert
-  // index among the lanes holding it (every remaining key is >= 1, so a lane
-  // with nothing left, head key 0, never matches); the winning lane moves to
-  // its second best, or, if that is not known, rescans its slots
+  // reduction 3, k rounds: the largest remaining key, then the lowest lane
+  // holding it (= the lowest expert index: lanes hold ascending blocks, and a
+  // lane's best is its lowest slot among equal keys). Every remaining key is
+  // >= 1, so a lane with nothing left (best key 0) never matches.
   int ri = 0;
   uint32_t rk = 0u;
   for (int r = 0; r < k; ++r) {
     if (r > 0) wk = __reduce_max_sync(0xffffffffu, k1);
-    const int my_e = lane + 32 * s1;
-    const bool mine = k1 == wk;
-    const int wi = __reduce_min_sync(0xffffffffu, mine ? my_e : 0x7fffffff);
-    if (mine && wi == my_e) {
+    const uint32_t hold = __ballot_sync(0xffffffffu, k1 == wk);
+    const int wl = __ffs(hold) - 1;
+    const int wi = wl * EPL + __shfl_sync(0xffffffffu, s1, wl);
+    if (lane == wl) {
       taken |= 1u << s1;
       if (second_known) {
         k1 = k2;
@@ -160,100 +186,13 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const T* __restrict__ lo
   route_store(lane, t, k, renorm, rk, ri, m, s, idx_out, w_out, lse_out);
 }
 
-// Compare-exchange for a descending order of (key, then lower slot first).
-__device__ __forceinline__ void cex(uint32_t& ka, uint32_t& sa, uint32_t& kb, uint32_t& sb) {
-  const bool sw = kb > ka || (kb == ka && sb < sa);
-  const uint32_t k0 = sw ? kb : ka, s0 = sw ? sb : sa;
-  kb = sw ? ka : kb;
-  sb = sw ? sa : sb;
-  ka = k0;
-  sa = s0;
-}
-
-// Sorting networks on 2, 4 and 8 inputs (1, 5 and 19 comparators; the
-// 8-input one has depth 6), checked on every 0-1 input.
-template <int EPL>
-__device__ __forceinline__ void sort_lane(uint32_t (&k)[EPL], uint32_t (&s)[EPL]) {
-#define RF_CEX(a, b) cex(k[a], s[a], k[b], s[b])
-  if constexpr (EPL == 2) {
-    RF_CEX(0, 1);
-  } else if constexpr (EPL == 4) {
-    RF_CEX(0, 1); RF_CEX(2, 3); RF_CEX(0, 2); RF_CEX(1, 3); RF_CEX(1, 2);
-  } else {
-    static_assert(EPL == 8, "sorted lanes hold 2, 4 or 8 experts");
-    RF_CEX(0, 2); RF_CEX(1, 3); RF_CEX(4, 6); RF_CEX(5, 7);
-    RF_CEX(0, 4); RF_CEX(1, 5); RF_CEX(2, 6); RF_CEX(3, 7);
-    RF_CEX(0, 1); RF_CEX(2, 3); RF_CEX(4, 5); RF_CEX(6, 7);
-    RF_CEX(2, 4); RF_CEX(3, 5);
-    RF_CEX(1, 4); RF_CEX(3, 6);
-    RF_CEX(1, 2); RF_CEX(3, 4); RF_CEX(5, 6);
-  }
-#undef RF_CEX
-}
-
-// Up to 8 experts per lane: each lane sorts its slots once; a round's
-// winning lane pops the head of its sorted list (no rescan).
-template <typename T, int EPL>
-__global__ void __launch_bounds__(256) moe_route_sorted_kernel(
-    const T* __restrict__ logits, int64_t T_, int E, int k, int renorm,
-    int32_t* __restrict__ idx_out, float* __restrict__ w_out, float* __restrict__ lse_out) {
-  const int lane = threadIdx.x & 31;
-  const int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T_) return;  // whole warps leave together
-  const T* row = logits + t * E;
-  // real experts get keys >= 1; padding gets 0 and sorts last, never selected
-  float x[EPL];
-  uint32_t key[EPL], sl[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    x[i] = e < E ? load_f(row + e) : kNegInf;
-    key[i] = e < E ? max(order_key(x[i]), 1u) : 0u;
-    sl[i] = i;
-  }
-  sort_lane<EPL>(key, sl);
-  uint32_t packed = 0u;  // sorted slots, four bits each, head in the low bits
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) packed |= sl[i] << (4 * i);
-  // reduction 1: the maximum (the first round's winning key)
-  uint32_t wk = __reduce_max_sync(0xffffffffu, key[0]);
-  const float m = key_value(wk);
-  // reduction 2: sum of exp(x - m), as in moe_route_kernel
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) s += ex2_approx((x[i] - m) * kLog2e);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  // reduction 3, k rounds (every remaining key is >= 1, so an exhausted
-  // lane, whose head key is 0, never matches)
-  int ri = 0;
-  uint32_t rk = 0u;
-  for (int r = 0; r < k; ++r) {
-    if (r > 0) wk = __reduce_max_sync(0xffffffffu, key[0]);
-    const int my_e = lane + 32 * int(packed & 15u);
-    const int wi = __reduce_min_sync(0xffffffffu, key[0] == wk ? my_e : 0x7fffffff);
-    if (wi == my_e && key[0] == wk) {  // pop the head
-#pragma unroll
-      for (int i = 0; i < EPL - 1; ++i) key[i] = key[i + 1];
-      key[EPL - 1] = 0u;
-      packed >>= 4;
-    }
-    if (lane == r) {
-      ri = wi;
-      rk = wk;
-    }
-  }
-  route_store(lane, t, k, renorm, rk, ri, m, s, idx_out, w_out, lse_out);
-}
-
 template <typename T, int EPL>
 cudaError_t launch_route(const T* x, int64_t T_, int E, int k, int renorm, int32_t* idx,
                          float* w, float* lse, cudaStream_t s) {
   const unsigned blocks = static_cast<unsigned>((T_ + 7) / 8);
-  if constexpr (EPL <= 8)
-    moe_route_sorted_kernel<T, EPL><<<blocks, 256, 0, s>>>(x, T_, E, k, renorm, idx, w, lse);
-  else
-    moe_route_kernel<T, EPL><<<blocks, 256, 0, s>>>(x, T_, E, k, renorm, idx, w, lse);
+  // rows start 16-byte aligned when the base does and E fills whole vectors
+  const int vec = reinterpret_cast<uintptr_t>(x) % 16 == 0 && E % (16 / sizeof(T)) == 0;
+  moe_route_kernel<T, EPL><<<blocks, 256, 0, s>>>(x, T_, E, k, renorm, vec, idx, w, lse);
   return cudaGetLastError();
 }
 
