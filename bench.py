@@ -49,36 +49,36 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch from ncu captures (summarised under profiles/), valid only for the
 # kernel source they were taken on; any change to the source makes it null.
 TRAFFIC = {
-    # attn_tc_kernel<128, 0> on gqa_long: dram read 677.3 MB + write 505.0 MB
-    "attn_tc_gqa_long": {"digest": "8dc32d453b50a32d", "bytes": 1182318592,
+    # attn_tc_kernel<128, 0> on gqa_long: dram read 677.1 MB + write 505.1 MB
+    "attn_tc_gqa_long": {"digest": "fa18dbb3c21d0cc7", "bytes": 1182172416,
                          "sources": ("attn_tc.cu", "rf_device.cuh")},
-    # attn_tc_kernel<128, 0> on mha_prefill: dram read 404.2 MB + write 113.1 MB
-    "attn_tc_mha_prefill": {"digest": "8dc32d453b50a32d", "bytes": 517277696,
+    # attn_tc_kernel<128, 0> on mha_prefill: dram read 404.0 MB + write 112.9 MB
+    "attn_tc_mha_prefill": {"digest": "fa18dbb3c21d0cc7", "bytes": 516974336,
                             "sources": ("attn_tc.cu", "rf_device.cuh")},
-    # attn_tc_kernel<64, 1> on two_level: dram__bytes.sum.per_second x duration
-    "attn_tc_two_level": {"digest": "8dc32d453b50a32d", "bytes": 350505000,
+    # attn_tc_kernel<64, 1> on two_level: dram read 286.1 MB + write 64.2 MB
+    "attn_tc_two_level": {"digest": "fa18dbb3c21d0cc7", "bytes": 350214400,
                           "sources": ("attn_tc.cu", "rf_device.cuh")},
-    # attn_tc_kernel<64, 0> on block_sparse: dram read 201.5 MB + write 50.1 MB
-    "attn_tc_block_sparse": {"digest": "8dc32d453b50a32d", "bytes": 251527680,
+    # attn_tc_kernel<64, 0> on block_sparse: dram read 201.5 MB + write 49.9 MB
+    "attn_tc_block_sparse": {"digest": "fa18dbb3c21d0cc7", "bytes": 251335168,
                              "sources": ("attn_tc.cu", "rf_device.cuh")},
     # attn_tc_kernel<64, 1> (the selected block-wise kernel) on scattered_short:
-    # dram read 100.9 MB + write 11.8 MB
-    "attn_tc_scattered_short": {"digest": "8dc32d453b50a32d", "bytes": 112646656,
+    # dram read 100.9 MB + write 12.8 MB
+    "attn_tc_scattered_short": {"digest": "fa18dbb3c21d0cc7", "bytes": 113701888,
                                 "sources": ("attn_tc.cu", "rf_device.cuh")},
     # softmax_rows kernels: dram__bytes_read.sum + dram__bytes_write.sum
-    # (rows_64k: 1073.9 + 1014.1 MB; rows_1m, clusters of 8, second pass back
-    # to front: 1366.6 + 1013.9 MB)
-    "softmax_rows_64k": {"digest": "500902232009bba1", "bytes": 2088053504,
+    # (rows_64k: 1073.8 + 1013.9 MB; rows_1m, clusters of 8, three CTAs per SM,
+    # second pass back to front: 1113.2 + 1014.5 MB)
+    "softmax_rows_64k": {"digest": "70553e06eb3b0b5c", "bytes": 2087659776,
                          "sources": ("softmax_rows.cu", "rf_device.cuh")},
-    "softmax_rows_1m": {"digest": "b278a7aa1a83890f", "bytes": 2380536064,
+    "softmax_rows_1m": {"digest": "70553e06eb3b0b5c", "bytes": 2127690752,
                         "sources": ("softmax_rows.cu", "rf_device.cuh")},
-    # moe_route_sorted_kernel<float, 8>, row_moments_smem_kernel<float> and
+    # moe_route_kernel<float, 8>, row_moments_smem_kernel<float> and
     # inertia_kernel: dram__bytes_read.sum + dram__bytes_write.sum
-    "moe_route": {"digest": "b54809b53ed0e0ac", "bytes": 139782656,
+    "moe_route": {"digest": "0079b63ed45830e3", "bytes": 139984384,
                   "sources": ("cascades.cu", "rf_device.cuh")},
-    "row_moments": {"digest": "b54809b53ed0e0ac", "bytes": 1016471552,
+    "row_moments": {"digest": "0079b63ed45830e3", "bytes": 1016576000,
                     "sources": ("cascades.cu", "rf_device.cuh")},
-    "inertia": {"digest": "b54809b53ed0e0ac", "bytes": 1076627200,
+    "inertia": {"digest": "0079b63ed45830e3", "bytes": 1076683776,
                 "sources": ("cascades.cu", "rf_device.cuh")},
     # fp8_gemm_kernel (persistent) and rowquant_kernel<bf16> on the 8192^3
     # workload: dram__bytes_read.sum + dram__bytes_write.sum
@@ -89,9 +89,8 @@ TRAFFIC = {
     # mla_decode_kernel on the MLA workload: dram read 306.9 MB + write 102.8 MB
     "mla_decode": {"digest": "68dfa35ccfdc00b3", "bytes": 409670912,
                    "sources": ("mla_decode.cu", "rf_device.cuh")},
-    # decode_partials_kernel<128, 4> on decode_splitk: 6.1856 TB/s x 695.49 us
-    # (sources since then differ only by device helpers the kernel does not use)
-    "decode_partials_decode_splitk": {"digest": "4c12c369bc05677a", "bytes": 4302000000,
+    # decode_partials_kernel<128, 4> on decode_splitk: dram read 4295.3 MB + write 6.1 MB
+    "decode_partials_decode_splitk": {"digest": "79dd3dbbb44ea5c6", "bytes": 4301339648,
                                       "sources": ("decode.cu", "rf_device.cuh")},
 }
 
