@@ -148,7 +148,8 @@ rf_status rf_attn_fwd(const void *q, const void *k, const void *v, void *o, floa
  * cut into chunks of whole (batch, key/value-head group) slices -- independent
  * problems, so no merge is needed (the single-segment strategy per chunk) --
  * and chunk c's copy in, its kernel and the copy out of chunk c - 1 run
- * concurrently on two internal streams and the caller's stream.
+ * concurrently on internal streams (one for copies in, one for copies out,
+ * two for the kernels, so that consecutive chunks' kernels overlap).
  *  q, k, v, o, lse: host pointers in rf_attn_fwd's layouts; page-locked
  *      memory (cudaHostAlloc, torch pin_memory) lets the copies run
  *      asynchronously, pageable memory works but serialises them. lse may be
@@ -160,7 +161,7 @@ rf_status rf_attn_fwd(const void *q, const void *k, const void *v, void *o, floa
  *  blockmask: as for rf_attn_fwd (device lists).
  * Ordering: the copies start after the work already queued on `stream`, and
  * work queued on `stream` afterwards starts after the last copy out; the host
- * is not blocked (except by pageable copies). The library creates two streams
+ * is not blocked (except by pageable copies). The library creates four streams
  * and a few events per device on first use and keeps them.
  * Errors: those of rf_attn_fwd; RF_ERR_INVALID for NULL host pointers or a
  * short or misaligned workspace, or while the visited-tile debug buffer is

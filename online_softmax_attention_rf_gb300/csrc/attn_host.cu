@@ -6,14 +6,18 @@
 // independent problems of the same kind (RedFuser technical summary, section
 // 3: partitions of the single-segment strategy need no merge when they do not
 // share a reduction axis). Chunk c moves through three streams:
-//   copy-in stream:   Q_c, K_c, V_c host -> device slot c % 2
-//   caller's stream:  rf_attn_fwd on the slot
-//   copy-out stream:  O_c, LSE_c device slot -> host
+//   copy-in stream:      Q_c, K_c, V_c host -> device slot c % 2
+//   compute stream c % 2: rf_attn_fwd on the slot
+//   copy-out stream:     O_c, LSE_c device slot -> host
 // so that the copy-in of chunk c + 1, the kernel of chunk c and the copy-out
-// of chunk c - 1 run at the same time. Two slots of device workspace, owned by
-// the caller, hold the chunks in flight. Events order the streams; the
-// caller's stream waits for the last copy-out, so the call is ordered on it
-// like any other entry point and nothing here synchronises the host.
+// of chunk c - 1 run at the same time. The kernels of consecutive chunks are
+// on two streams, so the next chunk's CTAs start on the SMs that the current
+// chunk's last partial wave leaves idle (a chunk is a few waves; one CTA of
+// the attention kernel fills an SM's shared memory, so CTAs of the two
+// kernels never share an SM). Two slots of device workspace, owned by the
+// caller, hold the chunks in flight. Events order the streams; the caller's
+// stream waits for the last copy-out, so the call is ordered on it like any
+// other entry point and nothing here synchronises the host.
 #include <cstdio>
 #include <mutex>
 
@@ -59,7 +63,7 @@ SlotLayout slot_layout(int H, int Hkv, int Sq, int Sk, int d, int hkv_c, size_t 
 struct DeviceQueues {
   std::mutex mu;
   bool ready = false;
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, comp[2] = {nullptr, nullptr};
   cudaEvent_t entry = nullptr, loaded[2] = {nullptr, nullptr}, computed[2] = {nullptr, nullptr},
               stored[2] = {nullptr, nullptr};
 };
@@ -69,6 +73,8 @@ cudaError_t queues_init(DeviceQueues& Q) {
   if (Q.ready) return cudaSuccess;
   cudaError_t e = cudaStreamCreateWithFlags(&Q.in, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&Q.out, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+    e = cudaStreamCreateWithFlags(&Q.comp[i], cudaStreamNonBlocking);
   cudaEvent_t* evs[7] = {&Q.entry, &Q.loaded[0], &Q.loaded[1], &Q.computed[0],
                          &Q.computed[1], &Q.stored[0], &Q.stored[1]};
   for (int i = 0; i < 7 && e == cudaSuccess; ++i)
@@ -141,6 +147,7 @@ extern "C" rf_status rf_attn_fwd_host(const void* q, const void* k, const void* 
   RF_CK(cudaEventRecord(Qs.entry, s), "record");
   RF_CK(cudaStreamWaitEvent(Qs.in, Qs.entry, 0), "wait");
   RF_CK(cudaStreamWaitEvent(Qs.out, Qs.entry, 0), "wait");
+  for (int i = 0; i < 2; ++i) RF_CK(cudaStreamWaitEvent(Qs.comp[i], Qs.entry, 0), "wait");
   for (int c = 0; c < chunks; ++c) {
     const int slot = c & 1;
     const int b = c / per_b, g0 = (c % per_b) * hkv_c, h0 = g0 * G;
@@ -158,7 +165,8 @@ extern "C" rf_status rf_attn_fwd_host(const void* q, const void* k, const void* 
                             cudaMemcpyHostToDevice, Qs.in), "copy in");
     }
     RF_CK(cudaEventRecord(Qs.loaded[slot], Qs.in), "record");
-    RF_CK(cudaStreamWaitEvent(s, Qs.loaded[slot], 0), "wait");
+    cudaStream_t cs = Qs.comp[slot];
+    RF_CK(cudaStreamWaitEvent(cs, Qs.loaded[slot], 0), "wait");
     rf_blockmask bm_c;
     const rf_blockmask* bmp = nullptr;
     if (blockmask != nullptr) {
@@ -169,9 +177,10 @@ extern "C" rf_status rf_attn_fwd_host(const void* q, const void* k, const void* 
     }
     const rf_status st = rf_attn_fwd(base + L.q, base + L.k, base + L.v, base + L.o,
                                      lse ? reinterpret_cast<float*>(base + L.lse) : nullptr, 1,
-                                     hq_c, hkv_c, Sq, Sk, d, scale, causal, bmp, dt, stream);
+                                     hq_c, hkv_c, Sq, Sk, d, scale, causal, bmp, dt,
+                                     reinterpret_cast<rf_stream>(cs));
     if (st != RF_OK) return st;  // message set by rf_attn_fwd
-    RF_CK(cudaEventRecord(Qs.computed[slot], s), "record");
+    RF_CK(cudaEventRecord(Qs.computed[slot], cs), "record");
     RF_CK(cudaStreamWaitEvent(Qs.out, Qs.computed[slot], 0), "wait");
     RF_CK(cudaMemcpyAsync(static_cast<unsigned char*>(o) + q_off, base + L.o, q_bytes,
                           cudaMemcpyDeviceToHost, Qs.out), "copy out");
@@ -180,7 +189,9 @@ extern "C" rf_status rf_attn_fwd_host(const void* q, const void* k, const void* 
                             cudaMemcpyDeviceToHost, Qs.out), "copy out");
     RF_CK(cudaEventRecord(Qs.stored[slot], Qs.out), "record");
   }
-  // the caller's stream resumes after the last copy out
+  // the caller's stream resumes after the last copy out (which follows every
+  // kernel: each chunk's copy out waits for its kernel, and the copy-out
+  // stream is in order)
   RF_CK(cudaStreamWaitEvent(s, Qs.stored[(chunks - 1) & 1], 0), "wait");
 #undef RF_CK
   return set_last_error(RF_OK, "");
