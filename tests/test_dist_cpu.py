@@ -80,6 +80,13 @@ def test_reference_arm_under_torchrun_prints_once():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 1
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the same metric, unit, direction and workload as the product arm, so
+    # that the two lines compare
+    sys.path.insert(0, ROOT)
+    import bench
+    assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
+    assert line["higher_is_better"] is True
+    assert line["config"]["workload"] == bench.WORKLOAD
 
 
 def _shard_rank_main(rank, world, port, out_dir):
