@@ -9,18 +9,22 @@
 // Shape of the kernel (STOF, Méthodologie, row-wise kernel): the query is
 // split by rows, one warp owns one row, the reductions are warp shuffles and
 // no inter-warp synchronisation enters the arithmetic. The eight warps of a
-// CTA share 32-key K/V sub-tiles staged in shared memory. Masked 128 x 128
-// tiles are skipped entirely: the CTA walks the same tile list (dense range,
-// causal range, or block-sparse row) the tensor-core kernel walks; inside a
-// partial tile of a two-level mask each key's bit in its 8 x 8 inner block
-// decides (STOF, two-level storage format).
+// CTA share K/V sub-tiles of 32 * KPL keys staged in shared memory (KPL = 4,
+// 2, 1 keys per lane for d <= 64, 128, 256, so one staging round covers a
+// whole 128-key mask tile at d <= 64). Each lane scores its KPL keys as KPL
+// independent dot products (16-byte reads of K rows padded to d + 4 floats:
+// conflict-free); the warp's probabilities go to shared memory and each lane
+// accumulates its output columns from them with two partial sums. Masked
+// 128 x 128 tiles are skipped entirely: the CTA walks the same tile list
+// (dense range, causal range, or block-sparse row) the tensor-core kernel
+// walks; inside a partial tile of a two-level mask each key's bit in its
+// 8 x 8 inner block decides (STOF, two-level storage format).
 #include "rf_device.cuh"
 
 namespace rf {
 namespace {
 
 constexpr int kRows = 8;       // query rows (warps) per CTA
-constexpr int kSub = 32;       // keys per staged sub-tile
 constexpr int kTile = 128;     // mask tile side
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -35,14 +39,25 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Shared-memory floats for head dimension d and KPL keys per lane.
+__host__ __device__ constexpr int simt_smem_floats(int d, int kpl) {
+  return 32 * kpl * (d + 4)      // K sub-tile, rows padded
+         + 32 * kpl * d          // V sub-tile
+         + kRows * d             // the CTA's query rows
+         + kRows * 32 * kpl;     // each warp's probabilities
+}
+
 // DCH = ceil(d / 32): output columns owned by each lane (lane + 32 t).
-template <int DCH>
+// KPL: keys per lane in a sub-tile of 32 * KPL keys.
+template <int DCH, int KPL>
 __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArgs a) {
+  constexpr int kSub = 32 * KPL;
   extern __shared__ float smem[];
-  const int d = a.d, dp = a.d + 1;
-  float* Ks = smem;                 // [kSub][d + 1] (padded: conflict-free column walk)
-  float* Vs = Ks + kSub * dp;       // [kSub][d]
+  const int d = a.d, dk = a.d + 4;
+  float* Ks = smem;                 // [kSub][d + 4]
+  float* Vs = Ks + kSub * dk;       // [kSub][d]
   float* Qs = Vs + kSub * d;        // [kRows][d]
+  float* Ps = Qs + kRows * d;       // [kRows][kSub]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nrb = (a.Sq + kRows - 1) / kRows;
   const int rb = blockIdx.x % nrb;
@@ -55,6 +70,7 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArg
   const float* qg = static_cast<const float*>(a.q) + (int64_t(bh) * a.Sq + i) * d;
   const float* kg = static_cast<const float*>(a.k) + int64_t(b * a.Hkv + hk) * a.Sk * d;
   const float* vg = static_cast<const float*>(a.v) + int64_t(b * a.Hkv + hk) * a.Sk * d;
+  float* pw = Ps + warp * kSub;
 
   if (row_ok)
     for (int c = lane; c < d; c += 32) Qs[warp * d + c] = qg[c];
@@ -109,44 +125,69 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArg
           kv = *reinterpret_cast<const float4*>(kg + int64_t(key) * d + c);
           vv = *reinterpret_cast<const float4*>(vg + int64_t(key) * d + c);
         }
-        float* kd = Ks + r * dp + c;
-        kd[0] = kv.x; kd[1] = kv.y; kd[2] = kv.z; kd[3] = kv.w;
+        *reinterpret_cast<float4*>(Ks + r * dk + c) = kv;
         *reinterpret_cast<float4*>(Vs + r * d + c) = vv;
       }
       __syncthreads();
       if (!row_ok) continue;
-      // scores of this row against the 32 keys (lane j <-> key k0 + j)
-      const int key = k0 + lane;
-      float s = kNegInf;
-      bool vis = key < row_kend;
-      if (vis && pb >= 0) {
-        const int rr = i - qt * kTile, cc = key - kt * kTile;
-        const uint64_t w = a.bits[int64_t(pb) * 256 + (rr >> 3) * (kTile / 8) + (cc >> 3)];
-        vis = (w >> ((rr & 7) * 8 + (cc & 7))) & 1;
-      }
-      if (vis) {
-        float dot = 0.f;
-        const float* qr = Qs + warp * d;
-        const float* kr = Ks + lane * dp;
-        for (int c = 0; c < d; ++c) dot = fmaf(qr[c], kr[c], dot);
-        s = dot * a.scale;
-      }
-      // online update: m' = max(m, max s); alpha = exp(m - m'); p = exp(s - m')
-      const float mn = fmaxf(m, warp_max(s));
-      if (mn == kNegInf) continue;  // nothing visible to this row yet
-      const float alpha = (m == kNegInf) ? 0.f : expf(m - mn);
-      const float p = (s == kNegInf) ? 0.f : expf(s - mn);
-      l = l * alpha + warp_sum(p);
+      // scores of this row against keys k0 + lane + 32 j, j < KPL
+      float s[KPL];
+      bool vis[KPL];
 #pragma unroll
-      for (int t = 0; t < DCH; ++t) acc[t] *= alpha;
-      for (int j = 0; j < kSub; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, p, j);
+      for (int j = 0; j < KPL; ++j) {
+        const int key = k0 + lane + 32 * j;
+        vis[j] = key < row_kend;
+        if (vis[j] && pb >= 0) {
+          const int rr = i - qt * kTile, cc = key - kt * kTile;
+          const uint64_t w = a.bits[int64_t(pb) * 256 + (rr >> 3) * (kTile / 8) + (cc >> 3)];
+          vis[j] = (w >> ((rr & 7) * 8 + (cc & 7))) & 1;
+        }
+        s[j] = 0.f;
+      }
+      const float* qr = Qs + warp * d;
+      for (int c = 0; c < d; c += 4) {
+        const float4 q4 = *reinterpret_cast<const float4*>(qr + c);
 #pragma unroll
-        for (int t = 0; t < DCH; ++t) {
-          const int c = lane + 32 * t;
-          if (c < d) acc[t] = fmaf(pj, Vs[j * d + c], acc[t]);
+        for (int j = 0; j < KPL; ++j) {
+          const float4 k4 = *reinterpret_cast<const float4*>(Ks + (lane + 32 * j) * dk + c);
+          s[j] = fmaf(q4.x, k4.x, s[j]);
+          s[j] = fmaf(q4.y, k4.y, s[j]);
+          s[j] = fmaf(q4.z, k4.z, s[j]);
+          s[j] = fmaf(q4.w, k4.w, s[j]);
         }
       }
+      float smax = kNegInf;
+#pragma unroll
+      for (int j = 0; j < KPL; ++j) {
+        s[j] = vis[j] ? s[j] * a.scale : kNegInf;
+        smax = fmaxf(smax, s[j]);
+      }
+      // online update: m' = max(m, max s); alpha = exp(m - m'); p = exp(s - m')
+      const float mn = fmaxf(m, warp_max(smax));
+      if (mn == kNegInf) continue;  // nothing visible to this row yet
+      const float alpha = (m == kNegInf) ? 0.f : expf(m - mn);
+      float psum = 0.f;
+#pragma unroll
+      for (int j = 0; j < KPL; ++j) {
+        const float pj = (s[j] == kNegInf) ? 0.f : expf(s[j] - mn);
+        pw[lane + 32 * j] = pj;
+        psum += pj;
+      }
+      l = l * alpha + warp_sum(psum);
+      __syncwarp();
+#pragma unroll
+      for (int t = 0; t < DCH; ++t) {
+        const int c = lane + 32 * t;
+        if (c < d) {
+          float a0 = 0.f, a1 = 0.f;
+          for (int k = 0; k < kSub; k += 2) {
+            a0 = fmaf(pw[k], Vs[k * d + c], a0);
+            a1 = fmaf(pw[k + 1], Vs[(k + 1) * d + c], a1);
+          }
+          acc[t] = acc[t] * alpha + (a0 + a1);
+        }
+      }
+      __syncwarp();  // pw is rewritten by the next sub-tile
       m = mn;
     }
   }
@@ -172,17 +213,17 @@ __global__ void attn_fill_empty(uint32_t* o_words, int64_t n_words, float* lse, 
       lse[e] = kNegInf;
 }
 
-template <int DCH>
+template <int DCH, int KPL>
 cudaError_t launch_dch(const AttnArgs& a, cudaStream_t s) {
-  const size_t smem = size_t(kSub * (a.d + 1) + kSub * a.d + kRows * a.d) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(attn_simt_f32_kernel<DCH>,
+  const size_t smem = size_t(simt_smem_floats(a.d, KPL)) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(attn_simt_f32_kernel<DCH, KPL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int64_t nrb = (a.Sq + kRows - 1) / kRows;
   const int64_t grid = nrb * a.B * a.H;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  attn_simt_f32_kernel<DCH><<<static_cast<unsigned>(grid), kRows * 32, smem, s>>>(a);
+  attn_simt_f32_kernel<DCH, KPL><<<static_cast<unsigned>(grid), kRows * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -198,14 +239,14 @@ cudaError_t launch_attn_empty(const AttnArgs& a, size_t elem_bytes, cudaStream_t
 cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t s) {
   if (a.Sk == 0) return launch_attn_empty(a, sizeof(float), s);
   switch ((a.d + 31) / 32) {
-    case 1: return launch_dch<1>(a, s);
-    case 2: return launch_dch<2>(a, s);
-    case 3: return launch_dch<3>(a, s);
-    case 4: return launch_dch<4>(a, s);
-    case 5: return launch_dch<5>(a, s);
-    case 6: return launch_dch<6>(a, s);
-    case 7: return launch_dch<7>(a, s);
-    default: return launch_dch<8>(a, s);
+    case 1: return launch_dch<1, 4>(a, s);
+    case 2: return launch_dch<2, 4>(a, s);
+    case 3: return launch_dch<3, 2>(a, s);
+    case 4: return launch_dch<4, 2>(a, s);
+    case 5: return launch_dch<5, 1>(a, s);
+    case 6: return launch_dch<6, 1>(a, s);
+    case 7: return launch_dch<7, 1>(a, s);
+    default: return launch_dch<8, 1>(a, s);
   }
 }
 
