@@ -30,6 +30,14 @@ CASES = [
     (2, 4, 2, 150, 333, 64, True, "f32"),
     (1, 2, 1, 97, 40, 100, True, "f32"),
     (1, 1, 1, 64, 200, 256, False, "f32"),
+    # the SIMT kernel's other widths: 4 keys per lane (d <= 64), 2 (d <= 128),
+    # 1 (d <= 256), with ragged rows and keys, causal and grouped heads
+    (1, 2, 1, 45, 300, 4, True, "f32"),
+    (2, 2, 2, 130, 129, 32, False, "f32"),
+    (1, 4, 2, 200, 260, 128, True, "f32"),
+    (1, 1, 1, 70, 333, 160, False, "f32"),
+    (1, 2, 1, 33, 190, 200, True, "f32"),
+    (1, 1, 1, 9, 257, 224, False, "f32"),
 ]
 
 
