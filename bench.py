@@ -92,7 +92,7 @@ TRAFFIC = {
     "mla_decode": {"digest": "68dfa35ccfdc00b3", "bytes": 409670912,
                    "sources": ("mla_decode.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: dram read 4295.3 MB + write 6.1 MB
-    "decode_partials_decode_splitk": {"digest": "79dd3dbbb44ea5c6", "bytes": 4301339648,
+    "decode_partials_decode_splitk": {"digest": "59aa2004ed2470c5", "bytes": 4301380096,
                                       "sources": ("decode.cu", "rf_device.cuh")},
 }
 

@@ -253,8 +253,9 @@ size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d);
  *   LSE = log sum_s exp(lse_s),   O = sum_s exp(lse_s - LSE) * O_s.
  *  o_part float32 [rows, nsplit, d], lse_part float32 [rows, nsplit] (device);
  *  o [rows, d] of dtype out_dt; lse float32 [rows] (may be NULL).
- * Partials with lse_s = -inf contribute nothing; a row whose partials are all
- * -inf gets O = 0 and LSE = -inf. rows >= 0, nsplit >= 1, 1 <= d <= 1024.
+ * Partials with lse_s = -inf contribute nothing (their O_s may hold any bits,
+ * NaN included: it is never added); a row whose partials are all -inf gets
+ * O = 0 and LSE = -inf. rows >= 0, nsplit >= 1, 1 <= d <= 1024.
  */
 rf_status rf_splitk_merge(const float *o_part, const float *lse_part, void *o, float *lse,
                           int64_t rows, int nsplit, int d, rf_dtype out_dt,

@@ -384,19 +384,43 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const float LSE = (M != kNegInf) ? M + logf(tot) : kNegInf;
   const float* op = o_part + row * st.o_row;
+  // Loads of kBatch splits are issued before any of them is used, so a warp
+  // keeps kBatch requests in flight instead of one; the sums still run over
+  // s = 0, 1, 2, ... in order. A split whose weight is 0 is loaded but not
+  // added (its partial may hold anything).
+  constexpr int kBatch = 8;
   if constexpr (kVec4) {
     // lane owns columns [4c, 4c + 4) for c = lane, lane + 32, ...
     for (int c0 = 0; c0 < d; c0 += 128) {
       const int c = c0 + 4 * lane;
+      const bool live = c < d;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int s0 = 0; s0 < nsplit; s0 += 32) {
         const int s = s0 + lane;
         const float ls = s < nsplit ? lp[s * st.l_split] : kNegInf;
         const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
         const int n = min(32, nsplit - s0);
-        for (int k = 0; k < n; ++k) {
+        int k = 0;
+        for (; k + kBatch <= n; k += kBatch) {
+          float4 v[kBatch];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j)
+            v[j] = live ? *reinterpret_cast<const float4*>(op + int64_t(s0 + k + j) * st.o_split + c)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            const float wk = __shfl_sync(0xffffffffu, w, k + j);
+            if (wk != 0.f) {
+              acc.x = fmaf(wk, v[j].x, acc.x);
+              acc.y = fmaf(wk, v[j].y, acc.y);
+              acc.z = fmaf(wk, v[j].z, acc.z);
+              acc.w = fmaf(wk, v[j].w, acc.w);
+            }
+          }
+        }
+        for (; k < n; ++k) {
           const float wk = __shfl_sync(0xffffffffu, w, k);
-          if (c < d && wk != 0.f) {
+          if (live && wk != 0.f) {
             const float4 v = *reinterpret_cast<const float4*>(op + int64_t(s0 + k) * st.o_split + c);
             acc.x = fmaf(wk, v.x, acc.x);
             acc.y = fmaf(wk, v.y, acc.y);
@@ -405,7 +429,7 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
           }
         }
       }
-      if (c < d) {
+      if (live) {
         o[row * d + c] = static_cast<TO>(acc.x);
         o[row * d + c + 1] = static_cast<TO>(acc.y);
         o[row * d + c + 2] = static_cast<TO>(acc.z);
@@ -415,18 +439,30 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
   } else {
     for (int c0 = 0; c0 < d; c0 += 32) {
       const int c = c0 + lane;
+      const bool live = c < d;
       float acc = 0.f;
       for (int s0 = 0; s0 < nsplit; s0 += 32) {
         const int s = s0 + lane;
         const float ls = s < nsplit ? lp[s * st.l_split] : kNegInf;
         const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
         const int n = min(32, nsplit - s0);
-        for (int k = 0; k < n; ++k) {
+        int k = 0;
+        for (; k + kBatch <= n; k += kBatch) {
+          float v[kBatch];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) v[j] = live ? op[int64_t(s0 + k + j) * st.o_split + c] : 0.f;
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            const float wk = __shfl_sync(0xffffffffu, w, k + j);
+            if (wk != 0.f) acc = fmaf(wk, v[j], acc);
+          }
+        }
+        for (; k < n; ++k) {
           const float wk = __shfl_sync(0xffffffffu, w, k);
-          if (c < d && wk != 0.f) acc = fmaf(wk, op[int64_t(s0 + k) * st.o_split + c], acc);
+          if (live && wk != 0.f) acc = fmaf(wk, op[int64_t(s0 + k) * st.o_split + c], acc);
         }
       }
-      if (c < d) o[row * d + c] = static_cast<TO>(acc);
+      if (live) o[row * d + c] = static_cast<TO>(acc);
     }
   }
   if (lane == 0 && lse != nullptr) lse[row] = LSE;

@@ -90,6 +90,30 @@ def test_merge_matches_oracle(cuda_device, rows, nsplit, d):
     assert_close(ob, o_ref, 8e-3 * max(1.0, float(np.abs(o_ref).max())), "O bf16")
 
 
+
+@pytest.mark.parametrize("nsplit,d", [(20, 128), (40, 64), (13, 33)])
+def test_merge_ignores_payload_of_empty_splits(cuda_device, nsplit, d):
+    # splits in the 8-wide load batches and in the tail after them, with
+    # lse = -inf and a NaN/inf payload: the merged rows stay finite and equal
+    # the oracle's merge of the remaining splits
+    rows = 6
+    o_part, lse_part = _partials(rows, nsplit, d, 100 + nsplit)
+    empty = [1, 3, nsplit - 1, nsplit // 2]
+    for s in empty:
+        lse_part[0, s] = -np.inf
+        o_part[0, s, :] = np.nan
+        lse_part[4, s] = -np.inf
+        o_part[4, s, ::2] = np.inf
+    o_ref, lse_ref = oracle.merge_partials(np.nan_to_num(o_part, nan=0.0, posinf=0.0), lse_part)
+    for dt in (torch.float32, torch.bfloat16):
+        o, lse = api.splitk_merge(torch.from_numpy(o_part).cuda(),
+                                  torch.from_numpy(lse_part).cuda(), dt)
+        keep = [0, 1, 4, 5]                    # row 2 is all -inf, row 3 is shifted by +80
+        tol = TOL_F32 if dt == torch.float32 else 8e-3 * max(1.0, float(np.abs(o_ref).max()))
+        assert torch.isfinite(o.float()).all()
+        assert_close(o[keep], o_ref[keep], tol, "O")
+        assert_close(lse[keep], lse_ref[keep], TOL_F32, "LSE")
+
 SOFTMAX_SHAPES = [
     (7, 33), (64, 1000), (3, 1), (16, 16384), (2, 32768), (3, 40000), (2, 262144),
     (1, 300001), (2, 600000), (5, 4099), (300, 32768), (200, 40000)]
