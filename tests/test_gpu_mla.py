@@ -36,6 +36,9 @@ def _oracle(q, kv, scale, batches=None):
     (3, 513, 1, 1.0),       # 17 tiles in one split
     (1, 1, 1, 1.0),         # a single key
     (2, 700, 2, 4.0),       # q x 4: large scores, the running maximum moves, O is rescaled
+    (1, 64, 1, 1.0),        # exactly one 64-key tile
+    (2, 130, 1, 1.0),       # two full tiles and a 2-key tail
+    (1, 2049, 3, 1.0),      # more tiles per split than ring stages, ragged splits
 ])
 def test_mla_decode_matches_oracle(cuda_device, B, Sk, nsplit, amp):
     q, kv = inputs.make_mla(B, Sk, B * 100 + Sk)
