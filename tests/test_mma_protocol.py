@@ -292,3 +292,20 @@ def test_planted_order_deadlocks():
             found = True
             break
     assert found
+
+
+def test_protocol_completes_with_many_items_per_cta():
+    """The roles' loops take any number of items per CTA; chaining several
+    heads' double items in one CTA (CTA c taking double items c, c + grid,
+    ...) must complete too."""
+    rng = np.random.default_rng(5)
+    for _ in range(80):
+        nq, nk, nh = int(rng.integers(1, 9)), int(rng.integers(1, 12)), int(rng.integers(1, 4))
+        mask = rng.random((nh, nq, nk)) < rng.random()
+        pairs = (nq + 1) // 2
+        nx = ((pairs + 1) // 2) * nh
+        for grid in (1, 2, 3):
+            for c in range(min(grid, nx)):
+                items = [it for x in range(c, nx, grid) for it in _cta_items(pairs, x)]
+                assert _run_cta(mask, nq, items, int(rng.choice([5, 8])), bool(rng.integers(0, 2)),
+                                random.Random(int(rng.integers(1 << 30)))), (nq, nk, nh, grid)
