@@ -86,6 +86,49 @@ def test_attn_fwd_rejects(L, kw, expect):
     assert L.rf_last_error()
 
 
+def _rowwise(L, q=A, k=A, v=A, o=A, lse=A, B=1, H=4, Hkv=2, Sq=256, Sk=256, d=128, scale=0.1,
+             causal=0, bm=None, dt=api.RF_BF16):
+    return L.rf_attn_fwd_rowwise(q, k, v, o, lse, B, H, Hkv, Sq, Sk, d, scale, causal, bm, dt, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Hkv=3), api.RF_ERR_INVALID),
+    (dict(scale=0.0), api.RF_ERR_INVALID),
+    (dict(scale=math.nan), api.RF_ERR_INVALID),
+    (dict(causal=2), api.RF_ERR_INVALID),
+    (dict(B=0), api.RF_ERR_INVALID),
+    (dict(Sk=(1 << 30) + 1), api.RF_ERR_INVALID),
+    (dict(d=32, dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),   # row-wise head dims: 64, 128
+    (dict(d=256, dt=api.RF_F32), api.RF_ERR_UNSUPPORTED),
+    (dict(d=96), api.RF_ERR_UNSUPPORTED),
+    (dict(dt=7), api.RF_ERR_INVALID),
+    (dict(q=None), api.RF_ERR_INVALID),
+    (dict(v=MIS), api.RF_ERR_INVALID),
+    (dict(lse=A + 2), api.RF_ERR_INVALID),
+])
+def test_attn_fwd_rowwise_rejects(L, kw, expect):
+    # the row-wise entry shares rf_attn_fwd's checks, all before any CUDA call
+    assert _rowwise(L, **kw) == expect
+    assert L.rf_last_error()
+
+
+def test_attn_fwd_rowwise_rejects_bad_blockmask(L):
+    bm = api.RFBlockMask(128, 128, 2, 2, A, A, 0)
+    bm.nqt = 3
+    assert _rowwise(L, bm=ctypes.byref(bm)) == api.RF_ERR_INVALID
+    assert _rowwise(L, q=None, o=None, Sq=0) == api.RF_OK   # no query rows: nothing to do
+
+
+def test_decode_workspace_size_formula(L):
+    # o_part [B*H, nsplit, d] then lse_part [B*H, nsplit], float32, rounded up to 256 bytes
+    for B, H, nsplit, d in [(1, 1, 1, 64), (3, 5, 7, 128), (16, 32, 32, 128), (2, 128, 16, 512)]:
+        n = B * H * nsplit * (d + 1) * 4
+        assert L.rf_decode_workspace_bytes(B, H, nsplit, d) == (n + 255) // 256 * 256
+    for bad in [(0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 0)]:
+        assert L.rf_decode_workspace_bytes(*bad) == 0
+    assert L.rf_mla_decode_workspace_bytes(2, 16) == L.rf_decode_workspace_bytes(2, 128, 16, 512)
+
+
 def test_attn_fwd_empty_query_is_a_no_op(L):
     assert _attn(L, q=None, o=None, Sq=0) == api.RF_OK
 
