@@ -49,6 +49,18 @@ __host__ __device__ constexpr int simt_smem_floats(int d, int kpl) {
 
 // DCH = ceil(d / 32): output columns owned by each lane (lane + 32 t).
 // KPL: keys per lane in a sub-tile of 32 * KPL keys.
+// 16-byte asynchronous global -> shared copy; with `in` false nothing is
+// read and the 16 bytes are zero-filled. And the wait for all of this
+// thread's copies (a hardware wait, not a spin loop).
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool in) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(in ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
 template <int DCH, int KPL>
 __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArgs a) {
   constexpr int kSub = 32 * KPL;
@@ -116,18 +128,18 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArg
       const int k0 = kt * kTile + sub * kSub;
       if (k0 >= kend) break;
       __syncthreads();  // the previous sub-tile is consumed
+      // K and V rows by asynchronous 16-byte copies, all of a thread's in
+      // flight at once (keys past Sk are filled with zeros)
       const int d4 = d / 4;
       for (int e = threadIdx.x; e < kSub * d4; e += kRows * 32) {
         const int r = e / d4, c = (e % d4) * 4;
         const int key = k0 + r;
-        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-        if (key < a.Sk) {
-          kv = *reinterpret_cast<const float4*>(kg + int64_t(key) * d + c);
-          vv = *reinterpret_cast<const float4*>(vg + int64_t(key) * d + c);
-        }
-        *reinterpret_cast<float4*>(Ks + r * dk + c) = kv;
-        *reinterpret_cast<float4*>(Vs + r * d + c) = vv;
+        const bool in = key < a.Sk;
+        const int64_t off = in ? int64_t(key) * d + c : 0;
+        cp_async16_zfill(Ks + r * dk + c, kg + off, in);
+        cp_async16_zfill(Vs + r * d + c, vg + off, in);
       }
+      cp_async_wait_all();
       __syncthreads();
       if (!row_ok) continue;
       // scores of this row against keys k0 + lane + 32 j, j < KPL
