@@ -84,8 +84,10 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArg
   const float* vg = static_cast<const float*>(a.v) + int64_t(b * a.Hkv + hk) * a.Sk * d;
   float* pw = Ps + warp * kSub;
 
+  // the query row by asynchronous copies too: the first sub-tile's wait
+  // covers it, so Q, K and V cost one round trip
   if (row_ok)
-    for (int c = lane; c < d; c += 32) Qs[warp * d + c] = qg[c];
+    for (int c = 4 * lane; c < d; c += 128) cp_async16_zfill(Qs + warp * d + c, qg + c, true);
 
   // keys visible to the CTA's last row bound every tile it may touch
   const int64_t shift = int64_t(a.Sk) - a.Sq;  // bottom-right causal alignment
@@ -203,6 +205,7 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_f32_kernel(const AttnArg
       m = mn;
     }
   }
+  cp_async_wait_all();  // a row with no visible tile still issued its Q copies
   if (!row_ok) return;
   float* og = static_cast<float*>(a.o) + (int64_t(bh) * a.Sq + i) * d;
   const float inv = l > 0.f ? 1.f / l : 0.f;
