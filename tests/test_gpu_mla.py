@@ -39,6 +39,8 @@ def _oracle(q, kv, scale, batches=None):
     (1, 64, 1, 1.0),        # exactly one 64-key tile
     (2, 130, 1, 1.0),       # two full tiles and a 2-key tail
     (1, 2049, 3, 1.0),      # more tiles per split than ring stages, ragged splits
+    (2, 20, 20, 1.0),       # one key per split
+    (1, 130, 2, 8.0),       # q x 8: the running maximum jumps between tiles
 ])
 def test_mla_decode_matches_oracle(cuda_device, B, Sk, nsplit, amp):
     q, kv = inputs.make_mla(B, Sk, B * 100 + Sk)
