@@ -86,8 +86,12 @@ typedef enum {
  * bit 8 r + c = element (r, c) of the block (1 = attended). A partial tile is
  * attended only where its bit is set (and, with causal, causally visible).
  * tile_bits = NULL: every listed tile is full (bits is ignored).
- * row_ptr, col_idx, tile_bits and bits are device pointers owned by the
- * caller; the struct itself is read on the host during the call only.
+ * Work order (optional): cta_order, as rf_blockmask_cta_order writes it, is
+ * the order in which rf_attn_fwd's tensor-core kernel takes its work items
+ * (bf16 only; the other kernels ignore it). NULL: head-major order. Entries
+ * outside [0, items) are skipped and reported through rf_device_status.
+ * row_ptr, col_idx, tile_bits, bits and cta_order are device pointers owned
+ * by the caller; the struct itself is read on the host during the call only.
  * Zero-initialise the struct so that fields added later read as absent.
  */
 typedef struct {
@@ -100,6 +104,7 @@ typedef struct {
   int per_head;              /* 0 or 1 */
   const int32_t *tile_bits;  /* device, parallel to col_idx; NULL: all tiles full */
   const uint64_t *bits;      /* device, 256 words per partial tile */
+  const int32_t *cta_order;  /* device, optional: see rf_blockmask_cta_order; NULL: head-major */
 } rf_blockmask;
 
 /*
@@ -158,7 +163,8 @@ rf_status rf_attn_fwd(const void *q, const void *k, const void *v, void *o, floa
  *  ws: device workspace of at least rf_attn_fwd_host_workspace_bytes(...)
  *      bytes, 256-byte aligned, owned by the caller (two chunks in flight);
  *      no other call may use it until this one's work on `stream` is done.
- *  blockmask: as for rf_attn_fwd (device lists).
+ *  blockmask: as for rf_attn_fwd (device lists); its cta_order is not used
+ *             (each chunk of heads runs in head-major order).
  * Ordering: the copies start after the work already queued on `stream`, and
  * work queued on `stream` afterwards starts after the last copy out; the host
  * is not blocked (except by pageable copies). The library creates four streams
@@ -377,6 +383,31 @@ int rf_attn_choose_kernel(int B, int H, int Sq, int Sk, int d, int64_t listed_ti
 int rf_attn_estimate_us(int B, int H, int Sq, int Sk, int d, int64_t listed_tiles,
                         int64_t partial_tiles, int64_t visible_pairs, int num_sms,
                         double *block_us, double *row_us);
+
+/*
+ * Work order of rf_attn_fwd's tensor-core (bf16) kernel for a block-sparse or
+ * two-level mask. The kernel's work items are double items x in [0, items),
+ * items = B * H * ceil(pairs / 2) with pairs = ceil(nqt / 2): item x of head
+ * x / ceil(pairs / 2) holds the query-tile pair counted j = x % ceil(pairs / 2)
+ * from the top and the pair counted j from the bottom (about equal causal
+ * work). By default CTA c takes item c, head-major, so that a head's K and V
+ * stay in L2 while its CTAs run. A mask whose query tiles differ a lot in
+ * listed tiles (global tokens: query rows that attend to every key, as in
+ * STOF's sparse patterns) then leaves one long CTA per head spread over the
+ * grid, and the last of them sets the kernel's end. This call writes order[c]
+ * = the item CTA c takes: the items whose listed tiles exceed twice the mean
+ * first, then the others, both in head-major order (a stable partition, so a
+ * mask without such items keeps the default order).
+ *  bm    : the lists (row_ptr required; its cta_order field is ignored);
+ *  B, H, Sq: the attention the order is for (nqt = ceil(Sq/128) = bm->nqt);
+ *  order : device int32 [cap], cap >= rf_blockmask_cta_order_len(B, H, Sq).
+ * Listed tiles are counted before any causal truncation. Asynchronous on the
+ * stream. Errors: RF_ERR_INVALID (bad sizes or fields, order NULL or short),
+ * RF_ERR_CUDA.
+ */
+int64_t rf_blockmask_cta_order_len(int B, int H, int Sq);
+rf_status rf_blockmask_cta_order(const rf_blockmask *bm, int B, int H, int Sq, int32_t *order,
+                                 int64_t cap, rf_stream stream);
 
 /*
  * Multi-head latent attention (MLA) decode, absorbed form (RedFuser page,

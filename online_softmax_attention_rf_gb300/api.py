@@ -34,7 +34,7 @@ class RFBlockMask(ctypes.Structure):
     _fields_ = [("tile_q", ctypes.c_int), ("tile_k", ctypes.c_int), ("nqt", ctypes.c_int),
                 ("nkt", ctypes.c_int), ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p),
                 ("per_head", ctypes.c_int), ("tile_bits", ctypes.c_void_p),
-                ("bits", ctypes.c_void_p)]
+                ("bits", ctypes.c_void_p), ("cta_order", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -66,6 +66,8 @@ SIGNATURES = {
     "rf_blockmask_build": (_I, [_P, _I, _I, _I, _P, _P, _I64, _P]),
     "rf_blockmask_build_elements": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
     "rf_blockmask_counts": (_I, [ctypes.POINTER(RFBlockMask), _I, _I, _I, _I, _I, _P, _P]),
+    "rf_blockmask_cta_order_len": (_I64, [_I, _I, _I]),
+    "rf_blockmask_cta_order": (_I, [ctypes.POINTER(RFBlockMask), _I, _I, _I, _P, _I64, _P]),
     "rf_attn_fwd_rowwise": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
                                  ctypes.POINTER(RFBlockMask), _I, _P]),
     "rf_attn_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I64, _I64, _I64, _I]),
@@ -146,18 +148,38 @@ class BlockMask:
     ``per_head`` is 1 when each (batch, head) has its own lists. With the
     two-level form, ``tile_bits`` int32 (parallel to ``col_idx``, -1 = full
     tile) and ``bits`` uint64 viewed as int64 [partial tiles, 256].
+    ``cta_orders`` caches the tensor-core kernel's work order
+    (rf_blockmask_cta_order) per (B, H, Sq).
     """
 
     def __init__(self, row_ptr, col_idx, nqt, nkt, per_head, tile_bits=None, bits=None):
         self.row_ptr, self.col_idx = row_ptr, col_idx
         self.nqt, self.nkt, self.per_head = nqt, nkt, per_head
         self.tile_bits, self.bits = tile_bits, bits
+        self.cta_orders = {}
 
-    def as_struct(self):
+    def as_struct(self, order=None):
         return RFBlockMask(TILE, TILE, self.nqt, self.nkt, self.row_ptr.data_ptr(),
                            self.col_idx.data_ptr(), self.per_head,
                            self.tile_bits.data_ptr() if self.tile_bits is not None else None,
-                           self.bits.data_ptr() if self.bits is not None else None)
+                           self.bits.data_ptr() if self.bits is not None else None,
+                           order.data_ptr() if order is not None else None)
+
+    def cta_order(self, B, H, Sq):
+        """rf_blockmask_cta_order for an attention of B x H heads and Sq queries,
+        or None when it is the default order (then the kernel need not read it).
+        Computed on the current stream the first time (one device comparison,
+        read back), then cached."""
+        key = (B, H, Sq)
+        if key not in self.cta_orders:
+            n = int(lib().rf_blockmask_cta_order_len(B, H, Sq))
+            order = torch.empty(max(1, n), dtype=torch.int32, device=self.row_ptr.device)
+            bm = self.as_struct()
+            _check(lib().rf_blockmask_cta_order(ctypes.byref(bm), B, H, Sq, _ptr(order), n,
+                                                _stream()))
+            ident = torch.arange(order.numel(), dtype=torch.int32, device=order.device)
+            self.cta_orders[key] = None if torch.equal(order, ident) else order
+        return self.cta_orders[key]
 
     @classmethod
     def from_dense_elements(cls, elem_mask, device="cuda"):
@@ -343,7 +365,12 @@ def attn_fwd(q, k, v, scale=None, causal=False, blockmask=None, out=None, lse=No
     if lse is None and with_lse:
         lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
     _cuda(o, lse)
-    bm = ctypes.byref(blockmask.as_struct()) if blockmask is not None else None
+    bm = None
+    if blockmask is not None:
+        # the tensor-core kernel takes its work in the mask's order (long
+        # items first); the other kernels ignore the field
+        order = blockmask.cta_order(B, H, Sq) if kernel == "block" and Sq > 0 else None
+        bm = ctypes.byref(blockmask.as_struct(order))
     fn = lib().rf_attn_fwd if kernel == "block" else lib().rf_attn_fwd_rowwise
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Sq, Sk, d, float(scale),
               1 if causal else 0, bm, _dt(q), _stream()))

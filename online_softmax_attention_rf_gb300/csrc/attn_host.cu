@@ -171,6 +171,7 @@ extern "C" rf_status rf_attn_fwd_host(const void* q, const void* k, const void* 
     const rf_blockmask* bmp = nullptr;
     if (blockmask != nullptr) {
       bm_c = *blockmask;
+      bm_c.cta_order = nullptr;  // an order for the whole problem does not fit a chunk's grid
       if (bm_c.per_head && bm_c.row_ptr != nullptr)
         bm_c.row_ptr += (int64_t(b) * H + h0) * nqt;  // this chunk's heads
       bmp = &bm_c;

@@ -113,7 +113,10 @@ struct Bars {
   uint32_t tmem_base;
   int abort_flag;
   int issue_lock;  // held by a group while it pushes one block of MMAs
+  int item_x;      // this CTA's double item (the work order's entry), -1: none
 };
+static_assert(sizeof(Bars) <= Layout<64>::kBarBytes && sizeof(Bars) <= Layout<128>::kBarBytes,
+              "barrier block overflows its shared-memory slot");
 
 // Key-tile list of one query tile: dense/causal range or a block-sparse row.
 struct TileList {
@@ -133,6 +136,7 @@ struct Params {
   const int32_t* tile_bits;  // two-level mask: bitmap index per list entry, or nullptr
   const uint64_t* bits;      // 256 words (8 x 8 blocks) per partial tile
   int per_head, nqt, nkt, pairs;
+  const int32_t* cta_order;  // work order: CTA c takes double item cta_order[c]; nullptr: c
   __nv_bfloat16* o;
   float* lse;
   uint8_t* visited;
@@ -266,11 +270,25 @@ __device__ __forceinline__ void issue_pv(uint32_t tm_o, uint32_t tm_p, uint64_t 
 // (heavy under causal masking: later tiles see more keys) and the pair counted
 // j from the bottom (light), so every CTA carries about the same causal work
 // and the hardware's CTA scheduler balances the rest. CTAs run head-major,
-// which keeps each head's K/V in L2 while its CTAs run. Returns false when
-// the CTA has no k-th item.
-__device__ __forceinline__ bool cta_item(const Params& p, int k, int& bh, int& qt0) {
+// which keeps each head's K/V in L2 while its CTAs run; a mask's work order
+// (cta_order, rf_blockmask_cta_order) may move the long double items to the
+// front: x is the CTA's double item, read once at the kernel's start
+// (item_x), -1 for an order entry outside the double items. Returns false
+// when the CTA has no k-th item.
+__device__ __forceinline__ int item_of_cta(const Params& p) {
+  if (p.cta_order == nullptr) return static_cast<int>(blockIdx.x);
+  const int x = p.cta_order[blockIdx.x];
+  const int64_t n = int64_t((p.pairs + 1) / 2) * p.B * p.H;
+  if (x < 0 || x >= n) {
+    record_status(p.status, dev_code(kDevBadList, kKerAttnTc, 3));
+    return -1;
+  }
+  return x;
+}
+
+__device__ __forceinline__ bool cta_item(const Params& p, int x, int k, int& bh, int& qt0) {
+  if (x < 0) return false;
   const int half = (p.pairs + 1) / 2;
-  const int x = static_cast<int>(blockIdx.x);
   const int j = x % half;
   bh = x / half;
   if (k == 0) {
@@ -313,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bar.abort_flag = 0;
     bar.issue_lock = 0;
+    bar.item_x = item_of_cta(p);
     fence_barrier_init();
   }
   if (warp == kWarpLoad) {
@@ -321,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  const int cta_x = bar.item_x;
   tc_fence_after_sync();
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort_flag = &bar.abort_flag;
@@ -337,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_loads[2] = {0, 0};
       bool ok = true;
       int bh, qt0;
-      for (int item = 0; ok && cta_item(p, item, bh, qt0); ++item) {
+      for (int item = 0; ok && cta_item(p, cta_x, item, bh, qt0); ++item) {
         const int bk = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);
         UnionIter it{tile_list(p, bh, qt0, false), tile_list(p, bh, qt0 + 1, false)};
         const int nt[2] = {it.l0.n, it.l1.n};
@@ -450,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // has no key tile in it, release all of its entries).
     auto start_item = [&](int k) {
       started = k;
-      if (!cta_item(p, k, ibh, iqt0)) return;
+      if (!cta_item(p, cta_x, k, ibh, iqt0)) return;
       it = UnionIter{tile_list(p, ibh, iqt0, t == 0), tile_list(p, ibh, iqt0 + 1, t == 1)};
       n_iss = 0;
       const int n = t == 0 ? it.l0.n : it.l1.n;
@@ -473,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // The same items, lists and group barriers as the softmax warps.
     int bh, qt0;
-    for (int item = 0; cta_item(p, item, bh, qt0); ++item) {
+    for (int item = 0; cta_item(p, cta_x, item, bh, qt0); ++item) {
       const TileList list = tile_list(p, bh, qt0 + t, false);
       if (lane == 0 && started < item) start_item(item);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -567,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every exit from the loops below is decided at a group barrier that the
     // group's issuer warp joins too, so the five warps always leave together.
     int bh, qt0;
-    for (int item = 0; cta_item(p, item, bh, qt0); ++item) {
+    for (int item = 0; cta_item(p, cta_x, item, bh, qt0); ++item) {
       const int qt = qt0 + t;
       const int row = qt * kBM + r;
       const TileList list = tile_list(p, bh, qt, false);
@@ -827,6 +847,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s, const char** why) {
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.visited = a.visited;
+  p.cta_order = a.cta_order;
   p.status = a.status;
   const int64_t items = int64_t(p.pairs) * a.B * a.H;
   if (items > 0x7fffffffLL) {

@@ -251,6 +251,84 @@ __global__ void __launch_bounds__(256) tile_bits_kernel(const uint8_t* __restric
   bits[int64_t(p) * 256 + threadIdx.x] = w;
 }
 
+
+// The tensor-core attention kernel's work order for a mask. Double item x
+// (head n = x / half, j = x % half, half = ceil(pairs / 2)) holds the query-tile
+// pair counted j from the top and the pair counted j from the bottom; its
+// work is the number of tiles listed for those (up to four) query tiles.
+// order[c], c < items: the items whose work exceeds twice the mean (w * items
+// > 2 * total) first, then the others, both ascending -- a stable partition,
+// so without such items the order is the identity. One CTA of 1024 threads:
+// a sum, a count, then chunks of 1024 items with block-wide exclusive scans.
+__device__ __forceinline__ int64_t order_work(const int32_t* row_ptr, int per_head, int nqt,
+                                              int pairs, int half, int64_t x) {
+  const int64_t n = x / half;
+  const int j = static_cast<int>(x % half);
+  const int64_t base = per_head ? n * nqt : 0;
+  const int qa = 2 * (pairs - 1 - j), qb = 2 * j;
+  int64_t w = 0;
+  for (int t = 0; t < 2; ++t) {
+    if (qa + t < nqt) w += row_ptr[base + qa + t + 1] - row_ptr[base + qa + t];
+    if (qb != qa && qb + t < nqt) w += row_ptr[base + qb + t + 1] - row_ptr[base + qb + t];
+  }
+  return w;
+}
+
+__device__ __forceinline__ int64_t block_sum_1024(int64_t v, int64_t* sh) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();  // sh is reused by consecutive calls
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int64_t t = 0;
+  for (int w = 0; w < 32; ++w) t += sh[w];
+  return t;
+}
+
+__global__ void __launch_bounds__(1024) cta_order_kernel(const int32_t* __restrict__ row_ptr,
+                                                         int per_head, int nqt, int BH,
+                                                         int32_t* __restrict__ order,
+                                                         int64_t items) {
+  __shared__ int64_t sh[32];
+  __shared__ int wh[32], wl[32];
+  const int pairs = (nqt + 1) / 2, half = (pairs + 1) / 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t part = 0;
+  for (int64_t x = threadIdx.x; x < items; x += 1024)
+    part += order_work(row_ptr, per_head, nqt, pairs, half, x);
+  const int64_t total = block_sum_1024(part, sh);
+  int64_t nh = 0;
+  for (int64_t x = threadIdx.x; x < items; x += 1024)
+    nh += order_work(row_ptr, per_head, nqt, pairs, half, x) * items > 2 * total ? 1 : 0;
+  const int64_t heavy_total = block_sum_1024(nh, sh);
+  int64_t heavy_base = 0, light_base = heavy_total;
+  for (int64_t x0 = 0; x0 < items; x0 += 1024) {
+    const int64_t x = x0 + threadIdx.x;
+    const bool in = x < items;
+    const bool heavy = in && order_work(row_ptr, per_head, nqt, pairs, half, x) * items > 2 * total;
+    const bool light = in && !heavy;
+    const unsigned bh = __ballot_sync(0xffffffffu, heavy), bl = __ballot_sync(0xffffffffu, light);
+    __syncthreads();  // wh / wl of the previous chunk have been read
+    if (lane == 0) {
+      wh[warp] = __popc(bh);
+      wl[warp] = __popc(bl);
+    }
+    __syncthreads();
+    int ph = 0, pl = 0, th = 0, tl = 0;
+    for (int w = 0; w < 32; ++w) {
+      if (w < warp) {
+        ph += wh[w];
+        pl += wl[w];
+      }
+      th += wh[w];
+      tl += wl[w];
+    }
+    const unsigned below = (1u << lane) - 1u;
+    if (heavy) order[heavy_base + ph + __popc(bh & below)] = static_cast<int32_t>(x);
+    if (light) order[light_base + pl + __popc(bl & below)] = static_cast<int32_t>(x);
+    heavy_base += th;
+    light_base += tl;
+  }
+}
 }  // namespace
 
 // Inputs of the analytic kernel selector, counted over the tile lists the
@@ -335,6 +413,13 @@ __global__ void __launch_bounds__(256) blockmask_counts_kernel(
     for (int w = 0; w < 8; ++w) t += red[threadIdx.x][w];
     if (t != 0) atomicAdd(counts + threadIdx.x, t * static_cast<unsigned long long>(mult));
   }
+}
+
+cudaError_t launch_cta_order(const int32_t* row_ptr, int per_head, int nqt, int BH, int32_t* order,
+                             int64_t items, cudaStream_t s) {
+  if (items <= 0) return cudaSuccess;
+  cta_order_kernel<<<1, 1024, 0, s>>>(row_ptr, per_head, nqt, BH, order, items);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_blockmask_counts(const int32_t* row_ptr, const int32_t* col_idx,

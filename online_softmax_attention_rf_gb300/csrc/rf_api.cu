@@ -188,6 +188,8 @@ rf_status attn_prepare(const char* fn, const void* q, const void* k, const void*
       return fail(RF_ERR_INVALID, "%s: blockmask tile_bits without bits", fn);
     if (bm->bits != nullptr && !aligned(bm->bits, 8))
       return fail(RF_ERR_INVALID, "%s: blockmask bits must be 8-byte aligned", fn);
+    if (bm->cta_order != nullptr && !aligned(bm->cta_order, 4))
+      return fail(RF_ERR_INVALID, "%s: blockmask cta_order must be 4-byte aligned", fn);
   }
   if (Sq == 0) {
     *empty = true;
@@ -215,6 +217,7 @@ rf_status attn_prepare(const char* fn, const void* q, const void* k, const void*
   a.tile_bits = bm ? bm->tile_bits : nullptr;
   a.bits = bm && bm->tile_bits ? bm->bits : nullptr;
   a.nqt = nqt; a.nkt = nkt;
+  a.cta_order = bm ? bm->cta_order : nullptr;
   a.visited = visited;
   a.status = st;
   return ok();
@@ -464,6 +467,35 @@ rf_status rf_blockmask_counts(const rf_blockmask* bm, int B, int H, int Sq, int 
       bm ? bm->bits : nullptr, bm ? bm->per_head : 0, B, H, Sq, Sk, causal, counts,
       reinterpret_cast<cudaStream_t>(stream), st);
   if (e != cudaSuccess) return cuda_fail(e, "rf_blockmask_counts: launch");
+  return ok();
+}
+
+int64_t rf_blockmask_cta_order_len(int B, int H, int Sq) {
+  if (B < 1 || H < 1 || Sq < 1 || Sq > (1 << 30)) return 0;
+  const int64_t pairs = cdiv(cdiv(Sq, 128), 2);
+  return int64_t(B) * H * cdiv(pairs, 2);
+}
+
+rf_status rf_blockmask_cta_order(const rf_blockmask* bm, int B, int H, int Sq, int32_t* order,
+                                 int64_t cap, rf_stream stream) {
+  const char* fn = "rf_blockmask_cta_order";
+  if (B < 1 || H < 1 || Sq < 1 || Sq > (1 << 30))
+    return fail(RF_ERR_INVALID, "%s: bad sizes B=%d H=%d Sq=%d", fn, B, H, Sq);
+  if (bm == nullptr || bm->row_ptr == nullptr || !aligned(bm->row_ptr, 4))
+    return fail(RF_ERR_INVALID, "%s: blockmask with a 4-byte aligned row_ptr required", fn);
+  const int nqt = static_cast<int>(cdiv(Sq, 128));
+  if (bm->tile_q != 128 || bm->tile_k != 128 || bm->nqt != nqt)
+    return fail(RF_ERR_INVALID, "%s: blockmask tiles must be 128x128 with nqt = %d", fn, nqt);
+  if (bm->per_head != 0 && bm->per_head != 1)
+    return fail(RF_ERR_INVALID, "%s: blockmask per_head must be 0/1", fn);
+  const int64_t items = rf_blockmask_cta_order_len(B, H, Sq);
+  if (items > INT32_MAX) return fail(RF_ERR_INVALID, "%s: too many work items", fn);
+  if (order == nullptr || !aligned(order, 4) || cap < items)
+    return fail(RF_ERR_INVALID, "%s: order must be a 4-byte aligned device int32[%lld]", fn,
+                static_cast<long long>(items));
+  cudaError_t e = rf::launch_cta_order(bm->row_ptr, bm->per_head, nqt, B * H, order, items,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rf_blockmask_cta_order: launch");
   return ok();
 }
 

@@ -86,6 +86,7 @@ struct AttnArgs {
   const int32_t* tile_bits;
   const uint64_t* bits;
   int nqt, nkt;
+  const int32_t* cta_order;  // optional work order of the tensor-core kernel (nullptr: head-major)
   uint8_t* visited;  // optional debug output, [B*H*nqt*nkt]
   int* status;
 };
@@ -129,6 +130,10 @@ cudaError_t launch_moment_of_inertia(const float* points, const float* masses, i
                                      cudaStream_t s);
 cudaError_t launch_row_moments(const void* x, int64_t rows, int64_t cols, float eps, float* mean,
                                float* var, void* y, rf_dtype dt, cudaStream_t s);
+// order[c] for c < items: the double items whose listed tiles exceed twice
+// the mean first, then the others, both ascending (one CTA).
+cudaError_t launch_cta_order(const int32_t* row_ptr, int per_head, int nqt, int BH, int32_t* order,
+                             int64_t items, cudaStream_t s);
 cudaError_t launch_blockmask_counts(const int32_t* row_ptr, const int32_t* col_idx,
                                     const int32_t* tile_bits, const uint64_t* bits, int per_head,
                                     int B, int H, int Sq, int Sk, int causal, int64_t* counts,

@@ -396,3 +396,33 @@ def test_blockmask_counts_validation(L):
     assert f(ctypes.byref(bm), 1, 1, 128, 128, 0, A, None) == api.RF_ERR_INVALID  # NULL lists
     bm = api.RFBlockMask(64, 128, 1, 1, A, A, 0)
     assert f(ctypes.byref(bm), 1, 1, 128, 128, 0, A, None) == api.RF_ERR_INVALID  # tile side
+
+
+def test_blockmask_cta_order_validation(L):
+    # every invalid argument is refused before any CUDA call
+    f, n = L.rf_blockmask_cta_order, L.rf_blockmask_cta_order_len
+    # items = B * H * ceil(ceil(nqt / 2) / 2)
+    assert n(1, 1, 128) == 1 and n(2, 3, 2048) == 2 * 3 * 4 and n(1, 1, 640) == 2
+    assert n(0, 1, 128) == 0 and n(1, 1, 0) == 0
+    bm = api.RFBlockMask(128, 128, 16, 16, A, A, 0)
+    ok = dict(bm=ctypes.byref(bm), B=1, H=1, Sq=2048, order=A, cap=4)
+    def call(**kw):
+        a = dict(ok); a.update(kw)
+        return f(a["bm"], a["B"], a["H"], a["Sq"], a["order"], a["cap"], None)
+    assert call(B=0) == api.RF_ERR_INVALID
+    assert call(Sq=0) == api.RF_ERR_INVALID
+    assert call(bm=None) == api.RF_ERR_INVALID
+    assert call(order=None) == api.RF_ERR_INVALID
+    assert call(order=A + 2) == api.RF_ERR_INVALID                            # alignment
+    assert call(cap=3) == api.RF_ERR_INVALID                                  # 4 items needed
+    assert call(Sq=1000) == api.RF_ERR_INVALID                                # nqt 8 != 16
+    bad = api.RFBlockMask(128, 128, 16, 16, None, A, 0)
+    assert call(bm=ctypes.byref(bad)) == api.RF_ERR_INVALID                   # no row_ptr
+    bad = api.RFBlockMask(128, 128, 16, 16, A, A, 2)
+    assert call(bm=ctypes.byref(bad)) == api.RF_ERR_INVALID                   # per_head
+    assert L.rf_last_error()
+
+
+def test_attn_fwd_rejects_misaligned_cta_order(L):
+    bm = api.RFBlockMask(128, 128, 2, 2, A, A, 0, None, None, A + 2)
+    assert _attn(L, bm=ctypes.byref(bm)) == api.RF_ERR_INVALID
