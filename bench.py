@@ -88,8 +88,9 @@ TRAFFIC = {
                  "sources": ("fp8_gemm.cu", "rf_device.cuh")},
     "rowquant": {"digest": "1bd446f9ea742eee", "bytes": 167583744,
                  "sources": ("fp8_gemm.cu", "rf_device.cuh")},
-    # mla_decode_kernel on the MLA workload: dram read 306.8 MB + write 103.5 MB
-    "mla_decode": {"digest": "a11060c239f84876", "bytes": 410284032,
+    # mla_decode_kernel (persistent, 128-key tiles) on the MLA workload: dram
+    # read 310.0 MB + write 7.6 MB (the merge kernel reads the partials)
+    "mla_decode": {"digest": "bec3777b93cd0491", "bytes": 317687040,
                    "sources": ("mla_decode.cu", "rf_device.cuh")},
     # decode_partials_kernel<128, 4> on decode_splitk: dram read 4295.3 MB + write 6.1 MB
     "decode_partials_decode_splitk": {"digest": "59aa2004ed2470c5", "bytes": 4301380096,

@@ -259,8 +259,8 @@ size_t rf_decode_workspace_bytes(int B, int H, int nsplit, int d);
  *   LSE = log sum_s exp(lse_s),   O = sum_s exp(lse_s - LSE) * O_s.
  *  o_part float32 [rows, nsplit, d], lse_part float32 [rows, nsplit] (device);
  *  o [rows, d] of dtype out_dt; lse float32 [rows] (may be NULL).
- * Partials with lse_s = -inf contribute nothing (their O_s may hold any bits,
- * NaN included: it is never added); a row whose partials are all -inf gets
+ * Partials with lse_s = -inf contribute nothing (their O_s is not read and
+ * may hold any bits, NaN included); a row whose partials are all -inf gets
  * O = 0 and LSE = -inf. rows >= 0, nsplit >= 1, 1 <= d <= 1024.
  */
 rf_status rf_splitk_merge(const float *o_part, const float *lse_part, void *o, float *lse,
@@ -420,11 +420,15 @@ rf_status rf_blockmask_cta_order(const rf_blockmask *bm, int B, int H, int Sq, i
  *  o   : bf16 [B, 128, 512]; lse: float [B, 128] (natural log) or NULL;
  *  s = scale * q . kv over all 576 columns; o = softmax(s) v.
  * The keys are cut into nsplit contiguous segments (floor(Sk/nsplit) keys,
- * the last one takes the remainder; 1 <= nsplit <= Sk); per segment and per
- * half of the value columns one CTA computes the partial (O, LSE) on the
- * tensor cores, and the partials are merged by log-sum-exp (rf_splitk_merge)
- * in the caller's workspace (float, >= rf_mla_decode_workspace_bytes bytes:
- * o_part [B*128, nsplit, 512] then lse_part [B*128, nsplit]). All pointers
+ * the last one takes the remainder; 1 <= nsplit <= Sk). One CTA per SM, half
+ * of them per half of the value columns, takes a contiguous run of the
+ * B * nsplit segments; the segments of one batch element within a run are
+ * folded into one partial (O, LSE), computed on the tensor cores and stored
+ * in the slot of the first of them (the other slots get LSE = -inf). The
+ * partials are merged by log-sum-exp (rf_splitk_merge) in the caller's
+ * workspace (float, >= rf_mla_decode_workspace_bytes bytes: o_part
+ * [B*128, nsplit, 512] then lse_part [B*128, nsplit]). So nsplit sets the
+ * granularity at which keys are dealt to the SMs. All pointers
  * device, 16-byte aligned (lse 4). Errors: RF_ERR_INVALID for bad sizes,
  * NULL or misaligned pointers, a short workspace; a device wait that gives
  * up records RF_ERR_TIMEOUT in the device status word.

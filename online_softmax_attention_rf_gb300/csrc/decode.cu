@@ -18,6 +18,8 @@
 // dot products of a batch of keys against every query head of the group are
 // reduced across lanes by a reduce-scatter (halving exchange), which leaves
 // two finished scores per lane instead of broadcasting all of them.
+#include <type_traits>
+
 #include "rf_device.cuh"
 
 namespace rf {
@@ -364,14 +366,22 @@ __device__ __forceinline__ float merge_max(const float* lp, int nsplit, int64_t 
   return M;
 }
 
-template <typename TO, bool kVec4>
-__global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restrict__ o_part,
+// kCPW chunks (of 128 columns with float4 access, else 32) per warp, kBatch
+// live splits per round of loads: kCPW * kBatch loads in flight per lane.
+template <typename TO, bool kVec4, int kCPW, int kBatch>
+__global__ void __launch_bounds__(128, kCPW == 1 ? 8 : 4) splitk_merge_kernel(const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            TO* __restrict__ o,
                                                            float* __restrict__ lse, int64_t rows,
                                                            int nsplit, int d,
                                                            const MergeStrides st) {
-  const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // one warp per (row, group of kCPW chunks): a wide row's chunks load in
+  // parallel; each warp forms the row's weights itself
+  constexpr int kCols = kVec4 ? 128 : 32;
+  const int groups = (d + kCPW * kCols - 1) / (kCPW * kCols);
+  const int64_t wid = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t row = wid / groups;
+  const int group = static_cast<int>(wid - row * groups);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const float* lp = lse_part + row * st.l_row;
@@ -384,88 +394,76 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const float* __restri
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const float LSE = (M != kNegInf) ? M + logf(tot) : kNegInf;
   const float* op = o_part + row * st.o_row;
-  // Loads of kBatch splits are issued before any of them is used, so a warp
-  // keeps kBatch requests in flight instead of one; the sums still run over
-  // s = 0, 1, 2, ... in order. A split whose weight is 0 is loaded but not
-  // added (its partial may hold anything).
-  constexpr int kBatch = 8;
-  if constexpr (kVec4) {
-    // lane owns columns [4c, 4c + 4) for c = lane, lane + 32, ...
-    for (int c0 = 0; c0 < d; c0 += 128) {
-      const int c = c0 + 4 * lane;
-      const bool live = c < d;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < nsplit; s0 += 32) {
-        const int s = s0 + lane;
-        const float ls = s < nsplit ? lp[s * st.l_split] : kNegInf;
-        const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
-        const int n = min(32, nsplit - s0);
-        int k = 0;
-        for (; k + kBatch <= n; k += kBatch) {
-          float4 v[kBatch];
+  // The splits of weight 0 are neither loaded nor added (their partials may
+  // hold anything, or never have been written). The others are taken in
+  // batches of up to kBatch, in ascending order, found from a ballot of the
+  // weights; each batch's loads are issued before any of them is used, so a
+  // row with few live splits costs one round trip to memory.
+  using V = typename std::conditional<kVec4, float4, float>::type;
+  int c[kCPW];
+  bool col[kCPW];
+  V acc[kCPW];
 #pragma unroll
-          for (int j = 0; j < kBatch; ++j)
-            v[j] = live ? *reinterpret_cast<const float4*>(op + int64_t(s0 + k + j) * st.o_split + c)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < kCPW; ++i) {
+    c[i] = (group * kCPW + i) * kCols + (kVec4 ? 4 * lane : lane);
+    col[i] = c[i] < d;
+    acc[i] = V{};
+  }
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const int s = s0 + lane;
+    const float ls = s < nsplit ? lp[s * st.l_split] : kNegInf;
+    const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
+    unsigned live = __ballot_sync(0xffffffffu, w != 0.f);
+    while (live != 0u) {
+      int idx[kBatch];
 #pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            const float wk = __shfl_sync(0xffffffffu, w, k + j);
-            if (wk != 0.f) {
-              acc.x = fmaf(wk, v[j].x, acc.x);
-              acc.y = fmaf(wk, v[j].y, acc.y);
-              acc.z = fmaf(wk, v[j].z, acc.z);
-              acc.w = fmaf(wk, v[j].w, acc.w);
-            }
-          }
+      for (int j = 0; j < kBatch; ++j) {
+        idx[j] = live != 0u ? __ffs(live) - 1 : -1;  // warp-uniform
+        live &= live - 1u;
+      }
+      float wk[kBatch];
+      V v[kBatch][kCPW];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) wk[j] = __shfl_sync(0xffffffffu, w, idx[j] < 0 ? 0 : idx[j]);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+        for (int i = 0; i < kCPW; ++i) {
+          v[j][i] = V{};
+          if (col[i] && idx[j] >= 0)
+            v[j][i] = *reinterpret_cast<const V*>(op + int64_t(s0 + idx[j]) * st.o_split + c[i]);
         }
-        for (; k < n; ++k) {
-          const float wk = __shfl_sync(0xffffffffu, w, k);
-          if (live && wk != 0.f) {
-            const float4 v = *reinterpret_cast<const float4*>(op + int64_t(s0 + k) * st.o_split + c);
-            acc.x = fmaf(wk, v.x, acc.x);
-            acc.y = fmaf(wk, v.y, acc.y);
-            acc.z = fmaf(wk, v.z, acc.z);
-            acc.w = fmaf(wk, v.w, acc.w);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (idx[j] < 0) continue;
+#pragma unroll
+        for (int i = 0; i < kCPW; ++i) {
+          if constexpr (kVec4) {
+            acc[i].x = fmaf(wk[j], v[j][i].x, acc[i].x);
+            acc[i].y = fmaf(wk[j], v[j][i].y, acc[i].y);
+            acc[i].z = fmaf(wk[j], v[j][i].z, acc[i].z);
+            acc[i].w = fmaf(wk[j], v[j][i].w, acc[i].w);
+          } else {
+            acc[i] = fmaf(wk[j], v[j][i], acc[i]);
           }
         }
       }
-      if (live) {
-        o[row * d + c] = static_cast<TO>(acc.x);
-        o[row * d + c + 1] = static_cast<TO>(acc.y);
-        o[row * d + c + 2] = static_cast<TO>(acc.z);
-        o[row * d + c + 3] = static_cast<TO>(acc.w);
-      }
-    }
-  } else {
-    for (int c0 = 0; c0 < d; c0 += 32) {
-      const int c = c0 + lane;
-      const bool live = c < d;
-      float acc = 0.f;
-      for (int s0 = 0; s0 < nsplit; s0 += 32) {
-        const int s = s0 + lane;
-        const float ls = s < nsplit ? lp[s * st.l_split] : kNegInf;
-        const float w = (ls == kNegInf || M == kNegInf) ? 0.f : expf(ls - LSE);
-        const int n = min(32, nsplit - s0);
-        int k = 0;
-        for (; k + kBatch <= n; k += kBatch) {
-          float v[kBatch];
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) v[j] = live ? op[int64_t(s0 + k + j) * st.o_split + c] : 0.f;
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            const float wk = __shfl_sync(0xffffffffu, w, k + j);
-            if (wk != 0.f) acc = fmaf(wk, v[j], acc);
-          }
-        }
-        for (; k < n; ++k) {
-          const float wk = __shfl_sync(0xffffffffu, w, k);
-          if (live && wk != 0.f) acc = fmaf(wk, op[int64_t(s0 + k) * st.o_split + c], acc);
-        }
-      }
-      if (live) o[row * d + c] = static_cast<TO>(acc);
     }
   }
-  if (lane == 0 && lse != nullptr) lse[row] = LSE;
+#pragma unroll
+  for (int i = 0; i < kCPW; ++i) {
+    if (!col[i]) continue;
+    TO* orow = o + row * d + c[i];
+    if constexpr (kVec4) {
+      orow[0] = static_cast<TO>(acc[i].x);
+      orow[1] = static_cast<TO>(acc[i].y);
+      orow[2] = static_cast<TO>(acc[i].z);
+      orow[3] = static_cast<TO>(acc[i].w);
+    } else {
+      orow[0] = static_cast<TO>(acc[i]);
+    }
+  }
+  if (lane == 0 && group == 0 && lse != nullptr) lse[row] = LSE;
 }
 
 template <int D, int GP>
@@ -510,25 +508,30 @@ cudaError_t launch_splitk_merge_strided(const float* o_part, const float* lse_pa
                                         int64_t o_split, int64_t o_row, int64_t l_split,
                                         int64_t l_row, rf_dtype out_dt, cudaStream_t s) {
   const int warps = 4;
-  const int64_t grid = (rows + warps - 1) / warps;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const MergeStrides st{o_split, o_row, l_split, l_row};
   const bool vec = d % 4 == 0 && reinterpret_cast<uintptr_t>(o_part) % 16 == 0 &&
                    o_split % 4 == 0 && o_row % 4 == 0;
+  // rows up to 128 columns: one chunk per warp, eight live splits per round;
+  // wider rows (float4): four chunks per warp, four live splits per round
+  const bool wide = vec && d > 128;
+  const int64_t cols = !vec ? 32 : wide ? 512 : 128;   // columns per warp
+  const int64_t grid = (rows * ((d + cols - 1) / cols) + warps - 1) / warps;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned g = static_cast<unsigned>(grid);
-  if (out_dt == RF_F32) {
-    float* of = static_cast<float*>(o);
-    if (vec)
-      splitk_merge_kernel<float, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d, st);
+  const unsigned t = warps * 32;
+  auto run = [&](auto* out) {
+    using TO = typename std::remove_pointer<decltype(out)>::type;
+    if (wide)
+      splitk_merge_kernel<TO, true, 4, 4><<<g, t, 0, s>>>(o_part, lse_part, out, lse, rows, nsplit, d, st);
+    else if (vec)
+      splitk_merge_kernel<TO, true, 1, 8><<<g, t, 0, s>>>(o_part, lse_part, out, lse, rows, nsplit, d, st);
     else
-      splitk_merge_kernel<float, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, of, lse, rows, nsplit, d, st);
-  } else {
-    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
-    if (vec)
-      splitk_merge_kernel<__nv_bfloat16, true><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d, st);
-    else
-      splitk_merge_kernel<__nv_bfloat16, false><<<g, warps * 32, 0, s>>>(o_part, lse_part, ob, lse, rows, nsplit, d, st);
-  }
+      splitk_merge_kernel<TO, false, 1, 8><<<g, t, 0, s>>>(o_part, lse_part, out, lse, rows, nsplit, d, st);
+  };
+  if (out_dt == RF_F32)
+    run(static_cast<float*>(o));
+  else
+    run(static_cast<__nv_bfloat16*>(o));
   return cudaGetLastError();
 }
 

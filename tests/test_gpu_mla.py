@@ -41,6 +41,12 @@ def _oracle(q, kv, scale, batches=None):
     (1, 2049, 3, 1.0),      # more tiles per split than ring stages, ragged splits
     (2, 20, 20, 1.0),       # one key per split
     (1, 130, 2, 8.0),       # q x 8: the running maximum jumps between tiles
+    # more segments than CTAs per value half (one per two SMs): each CTA folds a
+    # run of segments, and runs cross batch elements
+    (10, 1000, 20, 1.0),    # runs of 2-3 segments of 50 keys
+    (100, 300, 3, 1.0),     # runs of ~4 segments over 2-3 batch elements
+    (1, 20000, 200, 4.0),   # one batch element, runs of 2-3 segments of 100 keys
+    (40, 4096, 16, 1.0),    # runs of 8-9 segments of 256 keys
 ])
 def test_mla_decode_matches_oracle(cuda_device, B, Sk, nsplit, amp):
     q, kv = inputs.make_mla(B, Sk, B * 100 + Sk)
@@ -48,7 +54,10 @@ def test_mla_decode_matches_oracle(cuda_device, B, Sk, nsplit, amp):
     scale = 1.0 / math.sqrt(192.0)
     o, lse = api.mla_decode(q.cuda(), kv.cuda(), nsplit, scale)
     assert api.device_status() == 0
-    o_ref, lse_ref = _oracle(q, kv, scale)
+    bs = None if B <= 10 else [0, 1, B // 2, B - 2, B - 1]   # sampled rows of large batches
+    o_ref, lse_ref = _oracle(q, kv, scale, bs)
+    if bs is not None:
+        o, lse = o[bs], lse[bs]
     assert_close(o, o_ref, TOL_BF16_O, "O")
     assert_close(lse, lse_ref, TOL_BF16_LSE, "LSE")
 

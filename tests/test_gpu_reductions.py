@@ -70,7 +70,13 @@ def _partials(rows, nsplit, d, seed):
     return o_part, lse_part
 
 
-@pytest.mark.parametrize("rows,nsplit,d", [(5, 4, 64), (37, 32, 128), (9, 7, 100), (4, 130, 33)])
+@pytest.mark.parametrize("rows,nsplit,d", [
+    (5, 4, 64), (37, 32, 128), (9, 7, 100), (4, 130, 33),
+    # rows wider than 128 columns: four 128-column chunks per warp, four live
+    # splits per round of loads (partial chunk groups at 260 and 1000)
+    (6, 16, 512), (5, 9, 260), (4, 40, 1024), (7, 5, 1000),
+    (5, 6, 513),              # no float4 access: 32-column chunks
+])
 def test_merge_matches_oracle(cuda_device, rows, nsplit, d):
     o_part, lse_part = _partials(rows, nsplit, d, rows)
     o, lse = api.splitk_merge(torch.from_numpy(o_part).cuda(), torch.from_numpy(lse_part).cuda(),
@@ -91,7 +97,7 @@ def test_merge_matches_oracle(cuda_device, rows, nsplit, d):
 
 
 
-@pytest.mark.parametrize("nsplit,d", [(20, 128), (40, 64), (13, 33)])
+@pytest.mark.parametrize("nsplit,d", [(20, 128), (40, 64), (13, 33), (16, 512), (37, 1000)])
 def test_merge_ignores_payload_of_empty_splits(cuda_device, nsplit, d):
     # splits in the 8-wide load batches and in the tail after them, with
     # lse = -inf and a NaN/inf payload: the merged rows stay finite and equal
