@@ -166,10 +166,9 @@ class BlockMask:
                            order.data_ptr() if order is not None else None)
 
     def cta_order(self, B, H, Sq):
-        """rf_blockmask_cta_order for an attention of B x H heads and Sq queries,
-        or None when it is the default order (then the kernel need not read it).
-        Computed on the current stream the first time (one device comparison,
-        read back), then cached."""
+        """rf_blockmask_cta_order for an attention of B x H heads and Sq queries:
+        computed on the current stream the first time, then cached (the
+        kernel reads one entry per CTA)."""
         key = (B, H, Sq)
         if key not in self.cta_orders:
             n = int(lib().rf_blockmask_cta_order_len(B, H, Sq))
@@ -177,8 +176,7 @@ class BlockMask:
             bm = self.as_struct()
             _check(lib().rf_blockmask_cta_order(ctypes.byref(bm), B, H, Sq, _ptr(order), n,
                                                 _stream()))
-            ident = torch.arange(order.numel(), dtype=torch.int32, device=order.device)
-            self.cta_orders[key] = None if torch.equal(order, ident) else order
+            self.cta_orders[key] = order
         return self.cta_orders[key]
 
     @classmethod

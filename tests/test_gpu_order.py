@@ -66,9 +66,8 @@ def test_order_is_identity_without_long_items(cuda_device):
     bm = api.BlockMask.from_dense(tm)
     expect, heavy = _expected_order(bm.row_ptr.cpu().numpy(), bm.per_head, bm.nqt, B, H)
     assert not heavy
-    # the binding keeps no order when it is the default one ...
-    assert bm.cta_order(B, H, S) is None
-    # ... which is what the library writes
+    assert bm.cta_order(B, H, S).cpu().numpy().tolist() == list(range(len(expect)))
+    # the library writes every entry
     n = int(api.lib().rf_blockmask_cta_order_len(B, H, S))
     order = torch.full((n,), -1, dtype=torch.int32, device="cuda")
     st = bm.as_struct()
