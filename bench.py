@@ -49,21 +49,21 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch from ncu captures (summarised under profiles/), valid only for the
 # kernel source they were taken on; any change to the source makes it null.
 TRAFFIC = {
-    # attn_tc_kernel<128, 0> on gqa_long: dram read 676.1 MB + write 504.6 MB
-    "attn_tc_gqa_long": {"digest": "83acc9b4b734e4b0", "bytes": 1180650752,
+    # attn_tc_kernel<128, 0> on gqa_long: dram read 677.6 MB + write 505.0 MB
+    "attn_tc_gqa_long": {"digest": "912cb81acc2699e7", "bytes": 1182629120,
                          "sources": ("attn_tc.cu", "rf_device.cuh")},
-    # attn_tc_kernel<128, 0> on mha_prefill: dram read 403.8 MB + write 112.7 MB
-    "attn_tc_mha_prefill": {"digest": "83acc9b4b734e4b0", "bytes": 516471040,
+    # attn_tc_kernel<128, 0> on mha_prefill: dram read 404.3 MB + write 112.8 MB
+    "attn_tc_mha_prefill": {"digest": "912cb81acc2699e7", "bytes": 517131008,
                             "sources": ("attn_tc.cu", "rf_device.cuh")},
-    # attn_tc_kernel<64, 1> on two_level: dram read 284.3 MB + write 55.1 MB
-    "attn_tc_two_level": {"digest": "83acc9b4b734e4b0", "bytes": 339411200,
+    # attn_tc_kernel<64, 1> on two_level: dram read 289.3 MB + write 49.3 MB
+    "attn_tc_two_level": {"digest": "912cb81acc2699e7", "bytes": 338543360,
                           "sources": ("attn_tc.cu", "rf_device.cuh")},
-    # attn_tc_kernel<64, 0> on block_sparse: dram read 201.5 MB + write 50.0 MB
-    "attn_tc_block_sparse": {"digest": "83acc9b4b734e4b0", "bytes": 251422464,
+    # attn_tc_kernel<64, 0> on block_sparse: dram read 201.5 MB + write 49.8 MB
+    "attn_tc_block_sparse": {"digest": "912cb81acc2699e7", "bytes": 251304960,
                              "sources": ("attn_tc.cu", "rf_device.cuh")},
     # attn_tc_kernel<64, 1> (the selected block-wise kernel) on scattered_short:
     # dram read 100.9 MB + write 12.9 MB
-    "attn_tc_scattered_short": {"digest": "83acc9b4b734e4b0", "bytes": 113767168,
+    "attn_tc_scattered_short": {"digest": "912cb81acc2699e7", "bytes": 113853952,
                                 "sources": ("attn_tc.cu", "rf_device.cuh")},
     # softmax_rows kernels: dram__bytes_read.sum + dram__bytes_write.sum
     # (rows_64k: 1073.8 + 1013.9 MB; rows_1m, clusters of 8, three CTAs per SM,

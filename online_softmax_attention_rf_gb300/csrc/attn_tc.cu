@@ -92,7 +92,10 @@ struct Layout {
   static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   static constexpr int kBarBytes = 256;
-  static constexpr int kBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  // a split item's hand-over from group 1 to group 0: m and l of 128 rows
+  static constexpr int kOffXch = kOffBar + kBarBytes;
+  static constexpr int kXchBytes = 2 * kBM * 4;
+  static constexpr int kBytes = kOffXch + kXchBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemS = 0;        // S0 at 0, S1 at 128
   static constexpr uint32_t kTmemO = 2 * kBN;  // O0 at 256, O1 at 256 + D
   // P_t: on S_t's first 64 columns at D = 128 (S_t is read into registers
@@ -114,17 +117,22 @@ struct Bars {
   int abort_flag;
   int issue_lock;  // held by a group while it pushes one block of MMAs
   int item_x;      // this CTA's double item (the work order's entry), -1: none
+  uint64_t split_ready;  // split item: group 1's O, m and l are final (its 4 softmax warps)
+  uint64_t split_read;   // split item: group 0 has read them (its 4 softmax warps)
 };
 static_assert(sizeof(Bars) <= Layout<64>::kBarBytes && sizeof(Bars) <= Layout<128>::kBarBytes,
               "barrier block overflows its shared-memory slot");
+static_assert(Layout<64>::kBytes <= 227 * 1024 && Layout<128>::kBytes <= 227 * 1024,
+              "attention shared memory exceeds a CTA's limit");
 
 // Key-tile list of one query tile: dense/causal range or a block-sparse row.
 struct TileList {
   const int32_t* cols;  // nullptr: range [0, n)
   int n;                // entries (after causal truncation and validation)
   const int32_t* tb;    // inner-level bitmap index per entry (-1: full); nullptr: all full
-  __device__ __forceinline__ int at(int i) const { return cols ? cols[i] : i; }
-  __device__ __forceinline__ int bitmap(int i) const { return tb ? tb[i] : -1; }
+  int stride = 1;       // 2 in a split item's view: every second entry of a list
+  __device__ __forceinline__ int at(int i) const { return cols ? cols[i * stride] : i; }
+  __device__ __forceinline__ int bitmap(int i) const { return tb ? tb[i * stride] : -1; }
 };
 
 struct Params {
@@ -286,20 +294,105 @@ __device__ __forceinline__ int item_of_cta(const Params& p) {
   return x;
 }
 
-__device__ __forceinline__ bool cta_item(const Params& p, int x, int k, int& bh, int& qt0) {
+// One work item of a CTA: the query tile of each softmax group (>= nqt: the
+// group has none), or, for a split item, one query tile for both groups,
+// which take alternate entries of its list and merge their states at the end.
+struct Item {
+  int bh;
+  int q0, q1;
+  bool split;
+  __device__ __forceinline__ int q(int t) const { return t ? q1 : q0; }
+};
+
+// Raw length of query tile qt's list (before any truncation); 0 past the end.
+__device__ __forceinline__ int list_len(const Params& p, int bh, int qt) {
+  if (qt >= p.nqt) return 0;
+  const int32_t* rp = p.row_ptr + (p.per_head ? int64_t(bh) * p.nqt : 0) + qt;
+  return rp[1] - rp[0];
+}
+
+// The k-th item of double item x: the pair (2 (pairs - 1 - j), + 1), then
+// the pair (2 j, + 1) when it differs. In launches with a two-level mask, a
+// pair whose one tile lists more than 3 times its partner's entries plus 8
+// (the query tile holding a mask's global rows, next to a band tile) becomes
+// two items: the long tile split over both groups, then the other tile alone.
+// Otherwise the long tile's group works alone while the other group idles
+// after its few tiles. Every role computes the same sequence. Returns false
+// when the CTA has no k-th item.
+template <bool kInner>
+__device__ bool cta_item(const Params& p, int x, int k, Item& it) {
   if (x < 0) return false;
   const int half = (p.pairs + 1) / 2;
   const int j = x % half;
-  bh = x / half;
-  if (k == 0) {
-    qt0 = 2 * (p.pairs - 1 - j);
-    return true;
+  it.bh = x / half;
+  it.split = false;
+  if constexpr (!kInner) {
+    if (k == 0) {
+      it.q0 = 2 * (p.pairs - 1 - j);
+      it.q1 = it.q0 + 1;
+      return true;
+    }
+    if (k == 1 && j != p.pairs - 1 - j) {
+      it.q0 = 2 * j;
+      it.q1 = it.q0 + 1;
+      return true;
+    }
+    return false;
   }
-  if (k == 1 && j != p.pairs - 1 - j) {
-    qt0 = 2 * j;
-    return true;
+  const int npairs = j != p.pairs - 1 - j ? 2 : 1;
+  int idx = 0;
+  for (int s = 0; s < npairs; ++s) {
+    const int a = s == 0 ? 2 * (p.pairs - 1 - j) : 2 * j, b = a + 1;
+    int lng = -1, shrt = -1;
+    if (p.row_ptr != nullptr) {
+      const int la = list_len(p, it.bh, a), lb = list_len(p, it.bh, b);
+      if (la > 3 * lb + 8) {
+        lng = a;
+        shrt = b;
+      } else if (lb > 3 * la + 8) {
+        lng = b;
+        shrt = a;
+      }
+    }
+    if (lng >= 0) {
+      if (idx++ == k) {
+        it.q0 = it.q1 = lng;
+        it.split = true;
+        return true;
+      }
+      if (shrt < p.nqt && idx++ == k) {
+        it.q0 = shrt;
+        it.q1 = p.nqt;
+        it.split = false;
+        return true;
+      }
+    } else if (idx++ == k) {
+      it.q0 = a;
+      it.q1 = b;
+      it.split = false;
+      return true;
+    }
   }
   return false;
+}
+
+// Group t's list in item `it`: its tile's list, or, for a split item, the
+// entries at positions t, t + 2, ... of the shared tile's list (only group
+// 0's view records list faults).
+template <bool kInner>
+__device__ __forceinline__ TileList group_list(const Params& p, const Item& it, int t,
+                                               bool record) {
+  if (!kInner || !it.split) return tile_list(p, it.bh, it.q(t), record);
+  TileList L = tile_list(p, it.bh, it.q0, record && t == 0);
+  if (L.cols != nullptr) {
+    L.cols += t;
+    if (L.tb != nullptr) L.tb += t;
+    L.n = (L.n - t + 1) / 2;
+    L.stride = 2;
+  } else {
+    L.n = 0;  // not reached: items are split only in launches with lists
+  }
+  return L;
 }
 
 // kInner: the launch carries a two-level mask (inner 8 x 8 bitmaps); the
@@ -332,6 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar.abort_flag = 0;
     bar.issue_lock = 0;
     bar.item_x = item_of_cta(p);
+    mbar_init(&bar.split_ready, 4);
+    mbar_init(&bar.split_read, 4);
     fence_barrier_init();
   }
   if (warp == kWarpLoad) {
@@ -356,10 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seq = 0;
       int q_loads[2] = {0, 0};
       bool ok = true;
-      int bh, qt0;
-      for (int item = 0; ok && cta_item(p, cta_x, item, bh, qt0); ++item) {
+      Item d;
+      for (int item = 0; ok && cta_item<kInner>(p, cta_x, item, d); ++item) {
+        const int bh = d.bh;
         const int bk = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);
-        UnionIter it{tile_list(p, bh, qt0, false), tile_list(p, bh, qt0 + 1, false)};
+        UnionIter it{group_list<kInner>(p, d, 0, false), group_list<kInner>(p, d, 1, false)};
         const int nt[2] = {it.l0.n, it.l1.n};
         int u;
         bool n0, n1;
@@ -387,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(&bar.q_full[t], L::kTileBytes);
               for (int c = 0; c < D / 64; ++c)
                 tma_load_3d(smem + L::kOffQ + t * L::kTileBytes + c * kChunk, &tm_q,
-                            &bar.q_full[t], c * 64, (qt0 + t) * kBM, bh);
+                            &bar.q_full[t], c * 64, d.q(t) * kBM, bh);
               ++q_loads[t];
             }
           }
@@ -424,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n_iss = 0;                       // entries of this item issued (QK) so far
     int started = -1;                    // last item whose first QK was issued
     bool issued_any = false;
-    int ibh = 0, iqt0 = 0;               // item the issuer is on
+    Item icur{};                         // item the issuer is on
 #define RF_WAIT(b, par, site)                                                        \
   mbar_wait(&bar.b, (par), p.status, dev_code(kDevTimeout, kKerAttnTc, site), abort_flag)
 #define RF_SLOT(sq) (static_cast<uint64_t>((((sq) % NS) * L::kTileBytes) >> 4))
@@ -464,14 +560,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++n_iss == n) mma_commit(&bar.q_empty[t]);  // the item's last read of Q_t
       vseq = kseq + 1;
       if (p.visited != nullptr)
-        p.visited[(int64_t(ibh) * p.nqt + iqt0 + t) * p.nkt + u] = 1;
+        p.visited[(int64_t(icur.bh) * p.nqt + icur.q(t)) * p.nkt + u] = 1;
     };
     // Item k: wait for its Q_t and issue its first QK (or, when this group
     // has no key tile in it, release all of its entries).
     auto start_item = [&](int k) {
       started = k;
-      if (!cta_item(p, cta_x, k, ibh, iqt0)) return;
-      it = UnionIter{tile_list(p, ibh, iqt0, t == 0), tile_list(p, ibh, iqt0 + 1, t == 1)};
+      if (!cta_item<kInner>(p, cta_x, k, icur)) return;
+      it = UnionIter{group_list<kInner>(p, icur, 0, t == 0),
+                     group_list<kInner>(p, icur, 1, t == 1)};
       n_iss = 0;
       const int n = t == 0 ? it.l0.n : it.l1.n;
       if (n == 0) {
@@ -492,9 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // The same items, lists and group barriers as the softmax warps.
-    int bh, qt0;
-    for (int item = 0; cta_item(p, cta_x, item, bh, qt0); ++item) {
-      const TileList list = tile_list(p, bh, qt0 + t, false);
+    Item d;
+    for (int item = 0; cta_item<kInner>(p, cta_x, item, d); ++item) {
+      const TileList list = group_list<kInner>(p, d, t, false);
       if (lane == 0 && started < item) start_item(item);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int jj = 0; jj < list.n; ++jj) {
@@ -583,14 +680,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int shift = p.Sk - p.Sq;       // Sq, Sk <= 2^30: no overflow below
     int j = 0;                           // S tiles consumed (all items)
     int o_items = 0;                     // items whose final P.V was waited for
+    int n_split = 0;                     // split items so far
     bool ok = true;
     // Every exit from the loops below is decided at a group barrier that the
     // group's issuer warp joins too, so the five warps always leave together.
-    int bh, qt0;
-    for (int item = 0; cta_item(p, cta_x, item, bh, qt0); ++item) {
-      const int qt = qt0 + t;
+    Item d;
+    for (int item = 0; cta_item<kInner>(p, cta_x, item, d); ++item) {
+      const int bh = d.bh;
+      const int qt = d.q(t);
       const int row = qt * kBM + r;
-      const TileList list = tile_list(p, bh, qt, false);
+      const TileList list = group_list<kInner>(p, d, t, false);
       const int row_lim = p.causal ? min(p.Sk, row + 1 + shift) : p.Sk;
       const int tile_first_lim = p.causal ? min(p.Sk, qt * kBM + 1 + shift) : p.Sk;
       float m_run = kNegInf, l_run = 0.f;
@@ -741,6 +840,88 @@ if constexpr (kInner) {
       // epilogue: O = acc / l, LSE = (m + log2 l) ln 2. The next item's first
       // P.V on O_t is issued only after this group's next P is written, i.e.
       // after the TMEM reads below.
+      if constexpr (kInner) {
+        if (d.split) {
+          // A split item: group 1's state over the odd entries goes to group
+          // 0 (m and l through shared memory, O_1 read from tensor memory in
+          // the same lanes), which merges it with its own over the even
+          // entries and writes the rows. Group 1 then waits until group 0 has
+          // read them before its next item can overwrite O_1. The waits are
+          // bounded like every other.
+          if (list.n > 0) {
+            ok = mbar_wait_warp(&bar.o_done[t], o_items & 1, p.status,
+                                dev_code(kDevTimeout, kKerAttnTc, 32), abort_flag);
+            ++o_items;
+          }
+          float* xm = reinterpret_cast<float*>(smem + L::kOffXch);
+          float* xl = xm + kBM;
+          const uint32_t sp = n_split & 1;
+          ++n_split;
+          if (t == 1) {
+            if (ok) {
+              tc_fence_after_sync();
+              xm[r] = m_run;
+              xl[r] = l_run;
+              tc_fence_before_sync();
+              __syncwarp();
+              if ((threadIdx.x & 31) == 0) mbar_arrive(&bar.split_ready);
+              ok = mbar_wait_warp(&bar.split_read, sp, p.status,
+                                  dev_code(kDevTimeout, kKerAttnTc, 34), abort_flag);
+            }
+          } else {
+            if (ok)
+              ok = mbar_wait_warp(&bar.split_ready, sp, p.status,
+                                  dev_code(kDevTimeout, kKerAttnTc, 35), abort_flag);
+            if (ok) {
+              tc_fence_after_sync();
+              const bool row_ok = row < p.Sq;
+              const float m1 = xm[r], l1 = xl[r];
+              const float m = fmaxf(m_run, m1);
+              const float a0 = m_run == kNegInf ? 0.f : ex2_approx(m_run - m);
+              const float a1 = m1 == kNegInf ? 0.f : ex2_approx(m1 - m);
+              const float l = a0 * l_run + a1 * l1;
+              const float inv = l > 0.f ? 1.f / l : 0.f;
+              // a group without entries leaves its O columns unwritten: its
+              // weight is 0 and its values are never used
+              const float w0 = a0 * inv, w1 = a1 * inv;
+              const uint32_t tm_o1 = tmem + L::kTmemO + D + lane_off;
+              __nv_bfloat16* og = p.o + (int64_t(bh) * p.Sq + row) * D;
+#pragma unroll 1
+              for (int c = 0; c < D; c += 32) {
+                uint32_t o0[32], o1[32];
+                tmem_ld32_wait(tm_o + c, o0);
+                tmem_ld32_wait(tm_o1 + c, o1);
+                if (row_ok) {
+                  float v[32];
+#pragma unroll
+                  for (int e = 0; e < 32; ++e)
+                    v[e] = (w0 != 0.f ? w0 * __uint_as_float(o0[e]) : 0.f) +
+                           (w1 != 0.f ? w1 * __uint_as_float(o1[e]) : 0.f);
+#pragma unroll
+                  for (int e = 0; e < 32; e += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(v[e], v[e + 1]);
+                    w.y = pack_bf16x2(v[e + 2], v[e + 3]);
+                    w.z = pack_bf16x2(v[e + 4], v[e + 5]);
+                    w.w = pack_bf16x2(v[e + 6], v[e + 7]);
+                    *reinterpret_cast<uint4*>(og + c + e) = w;
+                  }
+                }
+              }
+              tc_fence_before_sync();
+              if (row_ok && p.lse != nullptr)
+                p.lse[int64_t(bh) * p.Sq + row] = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
+              __syncwarp();
+              if ((threadIdx.x & 31) == 0) mbar_arrive(&bar.split_read);
+            }
+          }
+          if (group_sync_or(t, !ok)) {
+            ok = false;
+            break;
+          }
+          continue;
+        }
+      }
       const bool row_ok = row < p.Sq && qt < p.nqt;
       __nv_bfloat16* og = p.o + (int64_t(bh) * p.Sq + row) * D;
       if (list.n > 0) {

@@ -79,6 +79,7 @@ def _run_cta(mask, nqt, items, NS, late_commits, rng, planted=False):
     met = {"sm": [0, 0], "is": [0, 0]}   # arrivals at each tile's group barrier
     lock = [0]
     pending = []
+    split_ready, split_read = _Bar(1), _Bar(1)
 
     def commit(b):
         if late_commits:
@@ -87,8 +88,13 @@ def _run_cta(mask, nqt, items, NS, late_commits, rng, planted=False):
             b.arrive()
 
     def lists(k):
+        if len(items[k]) == 3:                   # explicit lists (l0, l1, split)
+            return items[k][0], items[k][1]
         bh, qt0 = items[k]
         return _tile_list(mask, bh, qt0, nqt), _tile_list(mask, bh, qt0 + 1, nqt)
+
+    def is_split(k):
+        return len(items[k]) == 3 and items[k][2]
 
     def producer():
         seq, q_loads = 0, [0, 0]
@@ -120,7 +126,7 @@ def _run_cta(mask, nqt, items, NS, late_commits, rng, planted=False):
         yield lambda: met[other][t] >= mine
 
     def softmax(t):
-        j, o_items = 0, 0
+        j, o_items, n_split = 0, 0, 0
         for k in range(len(items)):
             n = len(lists(k)[t])
             for _ in range(n):
@@ -133,6 +139,15 @@ def _run_cta(mask, nqt, items, NS, late_commits, rng, planted=False):
                 par = o_items & 1
                 yield lambda par=par: o_done[t].done(par)
                 o_items += 1
+            if is_split(k):                           # group 1 hands over to group 0
+                par = n_split & 1
+                n_split += 1
+                if t == 1:
+                    split_ready.arrive()
+                    yield lambda par=par: split_read.done(par)
+                else:
+                    yield lambda par=par: split_ready.done(par)
+                    split_read.arrive()
             yield from group_barrier(t, "sm")         # after the epilogue
 
     def issuer(t):
@@ -309,3 +324,44 @@ def test_protocol_completes_with_many_items_per_cta():
                 items = [it for x in range(c, nx, grid) for it in _cta_items(pairs, x)]
                 assert _run_cta(mask, nq, items, int(rng.choice([5, 8])), bool(rng.integers(0, 2)),
                                 random.Random(int(rng.integers(1 << 30)))), (nq, nk, nh, grid)
+
+
+def _cta_items_split(mask, nqt, pairs, x):
+    """The kernel's items for a launch with a two-level mask: a pair whose
+    one tile lists more than 3 times its partner's entries plus 8 becomes a
+    split item (both groups on the long tile, alternate entries) and then the
+    other tile alone."""
+    out = []
+    for bh, a in _cta_items(pairs, x):
+        la, lb = _tile_list(mask, bh, a, nqt), _tile_list(mask, bh, a + 1, nqt)
+        if len(la) > 3 * len(lb) + 8 or len(lb) > 3 * len(la) + 8:
+            lng, shrt = (la, lb) if len(la) > len(lb) else (lb, la)
+            short_tile = a + 1 if lng is la else a
+            out.append((lng[0::2], lng[1::2], True))
+            if short_tile < nqt:
+                out.append((shrt, [], False))
+        else:
+            out.append((la, lb, False))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_protocol_completes_with_split_items(seed):
+    """Masks with long query tiles (global rows) next to short ones: the
+    split items' alternating lists, the lone short tiles and the hand-over
+    between the two groups must complete in any timing."""
+    rng = np.random.default_rng(100 + seed)
+    n_split = 0
+    for _ in range(40):
+        nq, nk, nh = int(rng.integers(1, 9)), int(rng.integers(10, 40)), int(rng.integers(1, 3))
+        mask = rng.random((nh, nq, nk)) < 0.08
+        for h in range(nh):
+            mask[h, int(rng.integers(0, nq))] = True     # a global query tile
+        pairs = (nq + 1) // 2
+        nx = ((pairs + 1) // 2) * nh
+        for x in range(nx):
+            items = _cta_items_split(mask, nq, pairs, x)
+            n_split += sum(1 for it in items if it[2])
+            assert _run_cta(mask, nq, items, int(rng.choice([5, 8])), bool(rng.integers(0, 2)),
+                            random.Random(int(rng.integers(1 << 30)))), (nq, nk, nh, x)
+    assert n_split > 0
